@@ -1,0 +1,287 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, never against the oracle itself.
+
+Each test names the property it pins and the passage it comes from (page
+title and section).  Pages:
+  BASED  = "BASED: Simple linear attention language models balance the
+           recall-throughput tradeoff" (reading notes)
+  JRT    = "Just read twice: closing the recall gap for recurrent language
+           models" (reading notes)
+  LENGEN = "Understanding and Improving Length Generalization in Recurrent
+           Models" (reading notes)
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import quadratic
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(12345)
+
+
+def rnd(*shape, scale=1.0):
+    return RNG.standard_normal(shape) * scale
+
+
+def rel(a, r):
+    return float(np.max(np.abs(a - r)) / max(np.max(np.abs(r)), 1e-300))
+
+
+# ---------------------------------------------------------------- feature map
+def test_feature_dims():
+    """BASED sec. 2.3 table: full expansion 1 + d' + d'^2 = 273 at d' = 16."""
+    assert oracle.feature_dim(16) == 273
+    assert oracle.phi(np.zeros(16)).shape == (273,)
+    assert oracle.phi(np.zeros(8)).shape == (73,)
+
+
+def test_phi_explicit_entries():
+    """BASED sec. 2.3: phi = [1, xbar, vec(xbar xbar^T)/sqrt2], xbar = x/d'^(1/4)."""
+    x = rnd(16)
+    p = oracle.phi(x)
+    xb = x / 2.0
+    assert p[0] == 1.0
+    assert np.array_equal(p[1:17], xb)
+    for a in (0, 3, 15):
+        for b in (0, 7, 15):
+            assert p[17 + 16 * a + b] == pytest.approx(xb[a] * xb[b] / math.sqrt(2), rel=1e-15)
+
+
+def test_phi_kernel_identity():
+    """BASED sec. 2.3: phi(qbar).phi(kbar) = 1 + q.k/sqrt(d') + (q.k)^2/(2d')
+    on 10^4 random pairs (d' = 16) and for d' in {1, 2, 8}."""
+    for dk, n in ((16, 10000), (1, 500), (2, 500), (8, 500)):
+        q = rnd(n, dk)
+        k = rnd(n, dk)
+        lhs = np.array([oracle.phi(q[i]) @ oracle.phi(k[i]) for i in range(n)])
+        rhs = quadratic.kernel_closed_form(q, k)
+        assert np.max(np.abs(lhs - rhs) / np.abs(rhs)) < 1e-13
+
+
+def test_kernel_positive_minimum():
+    """BASED sec. 2.3: 1 + t + t^2/2 = ((t+1)^2 + 1)/2 >= 1/2 with equality at
+    t = -1, i.e. q.k = -sqrt(d') = -4 at d' = 16."""
+    q = np.zeros(16); k = np.zeros(16)
+    q[0] = 2.0; k[0] = -2.0                      # q.k = -4
+    assert oracle.phi(q) @ oracle.phi(k) == pytest.approx(0.5, abs=1e-15)
+    q = rnd(20000, 16, scale=3.0); k = rnd(20000, 16, scale=3.0)
+    vals = np.array([oracle.phi(q[i]) @ oracle.phi(k[i]) for i in range(0, 20000, 7)])
+    assert vals.min() >= 0.5 - 1e-12
+
+
+# ---------------------------------------------------------- hand-worked cases
+def test_golden_dk1_by_hand():
+    """tests/golden/hand_worked_dk1.json: two tokens at d' = 1 worked by hand."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_worked_dk1.json")))
+    q = np.array(g["q"])[None, None]; k = np.array(g["k"])[None, None]
+    v = np.array(g["v"])[None, None]
+    y, s, z = oracle.prefill(q, k, v)
+    np.testing.assert_allclose(y[0, 0], np.array(g["y"]), rtol=1e-15)
+    np.testing.assert_allclose(s[0, 0], np.array(g["s"]), rtol=1e-15)
+    np.testing.assert_allclose(z[0, 0], np.array(g["z"]), rtol=1e-15)
+
+
+def test_golden_dk16_by_hand():
+    """tests/golden/hand_worked_dk16.json: three tokens at d' = 16 by hand."""
+    g = json.load(open(os.path.join(GOLDEN, "hand_worked_dk16.json")))
+    N, dk, dv = 3, g["dk"], g["dv"]
+    q = np.zeros((1, 1, N, dk)); k = np.zeros((1, 1, N, dk))
+    for i in range(N):
+        for a, val in g["q_nonzero"][i]:
+            q[0, 0, i, a] = val
+        for a, val in g["k_nonzero"][i]:
+            k[0, 0, i, a] = val
+    v = np.array(g["v"])[None, None]
+    y, s, z = oracle.prefill(q, k, v)
+    np.testing.assert_allclose(y[0, 0], np.array(g["y"]), rtol=1e-15, atol=1e-15)
+    s_ref = np.zeros((273, dv)); z_ref = np.zeros(273)
+    for f, row in g["s_nonzero"].items():
+        s_ref[int(f)] = row
+    for f, val in g["z_nonzero"].items():
+        z_ref[int(f)] = val
+    np.testing.assert_allclose(s[0, 0], s_ref, rtol=1e-15, atol=1e-15)
+    np.testing.assert_allclose(z[0, 0], z_ref, rtol=1e-15, atol=1e-15)
+
+
+def test_tiny_brute_force():
+    """BASED sec. 2.2, Eq. (1): for N in {1,2,3} the outputs are the K-weighted
+    means written out token by token with scalar loops."""
+    dk, dv = 16, 5
+    for N in (1, 2, 3):
+        q = rnd(1, 1, N, dk); k = rnd(1, 1, N, dk); v = rnd(1, 1, N, dv)
+        y, _, _ = oracle.prefill(q, k, v)
+        for i in range(N):
+            w = []
+            for j in range(i + 1):
+                t = sum(q[0, 0, i, a] * k[0, 0, j, a] for a in range(dk))
+                w.append(1.0 + t / 4.0 + t * t / 32.0)
+            for c in range(dv):
+                ref = sum(w[j] * v[0, 0, j, c] for j in range(i + 1)) / sum(w)
+                assert y[0, 0, i, c] == pytest.approx(ref, rel=1e-12, abs=1e-14)
+        # one token: y_1 = v_1 up to a few ulps of fp64 rounding
+        assert rel(y[0, 0, 0], v[0, 0, 0]) < 1e-14
+
+
+# ------------------------------------------------------- recurrence vs forms
+def test_recurrent_equals_quadratic_closed_form():
+    """BASED sec. 2.2, Eq. (1) = Eqs. (2)-(3): recurrent form equals the O(N^2)
+    closed form, at the small fp32 workload's shape (B=1, H=2, N=256)."""
+    q = rnd(1, 2, 256, 16); k = rnd(1, 2, 256, 16); v = rnd(1, 2, 256, 64)
+    y, _, _ = oracle.prefill(q, k, v)
+    y_ref = quadratic.prefill_closed_form(q, k, v)
+    assert rel(y, y_ref) < 1e-12
+
+
+def test_running_mean_when_kernel_is_one():
+    """q = 0 or k = 0 makes K = 1 (BASED sec. 2.3), so y_i = mean(v_1..v_i)."""
+    N = 40
+    v = rnd(1, 1, N, 8)
+    mean = np.cumsum(v, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    for q, k in ((np.zeros((1, 1, N, 16)), rnd(1, 1, N, 16)),
+                 (rnd(1, 1, N, 16), np.zeros((1, 1, N, 16)))):
+        y, _, _ = oracle.prefill(q, k, v)
+        assert rel(y, mean) < 1e-13
+
+
+@pytest.mark.parametrize("C", [1, 16, 64, 100])
+def test_chunked_equals_recurrent(C):
+    """BASED sec. 2.5: the blockwise form is an exact re-association of the
+    recurrence, for block lengths that do and do not divide N, with s0."""
+    N = 203
+    q = rnd(1, 2, N, 16); k = rnd(1, 2, N, 16); v = rnd(1, 2, N, 64)
+    s0 = rnd(1, 2, 273, 64, scale=5.0); z0 = np.abs(rnd(1, 2, 273)) + 1.0
+    y, s, z = oracle.prefill(q, k, v, s0, z0)
+    yc, sc, zc = oracle.prefill_chunked(q, k, v, C, s0, z0)
+    assert rel(yc, y) < 1e-12 and rel(sc, s) < 1e-12 and rel(zc, z) < 1e-12
+
+
+# ------------------------------------------------------------ state invariants
+def test_state_invariants():
+    """BASED sec. 2.5 (order-0 term = prefix sum of v) and the definition of z:
+    z_N[0] = z0[0] + N, s_N[0,:] = s0[0,:] + sum v, z_N[1+a] = z0[1+a] + sum k_a/2,
+    and the quadratic block of s - s0 is symmetric in (a, b)."""
+    N = 97
+    q = rnd(2, 3, N, 16); k = rnd(2, 3, N, 16); v = rnd(2, 3, N, 64)
+    s0 = rnd(2, 3, 273, 64); z0 = np.abs(rnd(2, 3, 273)) + 1.0
+    _, s, z = oracle.prefill(q, k, v, s0, z0)
+    np.testing.assert_allclose(z[..., 0], z0[..., 0] + N, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(s[..., 0, :], s0[..., 0, :] + v.sum(axis=2), atol=1e-11)
+    np.testing.assert_allclose(z[..., 1:17], z0[..., 1:17] + k.sum(axis=2) / 2.0, atol=1e-11)
+    dq = (s - s0)[..., 17:, :].reshape(2, 3, 16, 16, 64)
+    np.testing.assert_allclose(dq, np.swapaxes(dq, 2, 3), atol=1e-11)
+    # quadratic block of z: sum_j kbar_a kbar_b / sqrt2
+    zq = (z - z0)[..., 17:].reshape(2, 3, 16, 16)
+    gram = np.einsum("bhna,bhnc->bhac", k / 2.0, k / 2.0) / math.sqrt(2.0)
+    np.testing.assert_allclose(zq, gram, atol=1e-11)
+
+
+def test_state_passing_split_equals_whole():
+    """LENGEN sec. 2.5, Eq. (4) with A_t = I: running N1 tokens, then N2 tokens
+    from the resulting state, equals one run over N1 + N2 tokens."""
+    N1, N2 = 70, 53
+    q = rnd(1, 2, N1 + N2, 16); k = rnd(1, 2, N1 + N2, 16); v = rnd(1, 2, N1 + N2, 64)
+    y, s, z = oracle.prefill(q, k, v)
+    y1, s1, z1 = oracle.prefill(q[:, :, :N1], k[:, :, :N1], v[:, :, :N1])
+    y2, s2, z2 = oracle.prefill(q[:, :, N1:], k[:, :, N1:], v[:, :, N1:], s1, z1)
+    assert rel(np.concatenate([y1, y2], axis=2), y) < 1e-12
+    assert rel(s2, s) < 1e-12 and rel(z2, z) < 1e-12
+
+
+def test_initial_state_against_closed_form():
+    """LENGEN sec. 2.5, Eq. (4): an initial state adds phi(q_i).s0 to every
+    numerator and phi(q_i).z0 to every denominator.  s0/z0 come from a prefix
+    sequence, so the reference is the closed form over the concatenation."""
+    Np, N = 37, 51
+    q = rnd(1, 1, Np + N, 16); k = rnd(1, 1, Np + N, 16); v = rnd(1, 1, Np + N, 8)
+    _, s0, z0 = oracle.prefill(q[:, :, :Np], k[:, :, :Np], v[:, :, :Np])
+    y, _, _ = oracle.prefill(q[:, :, Np:], k[:, :, Np:], v[:, :, Np:], s0, z0)
+    y_ref = quadratic.prefill_closed_form(q, k, v)[:, :, Np:]
+    assert rel(y, y_ref) < 1e-12
+
+
+def test_decode_steps_equal_prefill():
+    """BASED sec. 2.2: decode is one step of the same recurrence, so n decode
+    steps from (s0, z0) reproduce the prefill of those n tokens."""
+    n = 9
+    q = rnd(2, 2, n, 16); k = rnd(2, 2, n, 16); v = rnd(2, 2, n, 64)
+    s0 = rnd(2, 2, 273, 64); z0 = np.abs(rnd(2, 2, 273)) + 3.0
+    y, s, z = oracle.prefill(q, k, v, s0, z0)
+    ss, zz = s0, z0
+    for i in range(n):
+        yi, ss, zz = oracle.decode_step(q[:, :, i], k[:, :, i], v[:, :, i], ss, zz)
+        assert rel(yi, y[:, :, i]) < 1e-13
+    assert rel(ss, s) < 1e-13 and rel(zz, z) < 1e-13
+
+
+def test_eps_enters_denominator_only():
+    """The eps the implementation adds (BASED sec. 2.3) shifts the denominator."""
+    q = rnd(1, 1, 5, 16); k = rnd(1, 1, 5, 16); v = rnd(1, 1, 5, 4)
+    y0, _, _ = oracle.prefill(q, k, v)
+    y1, _, _ = oracle.prefill(q, k, v, eps=0.5)
+    y_ref = quadratic.prefill_closed_form(q, k, v, eps=0.5)
+    assert rel(y1, y_ref) < 1e-13 and not np.allclose(y0, y1)
+
+
+# ------------------------------------------------------------------- prefix
+def test_prefix_zero_length_is_causal():
+    """JRT sec. 2.6: with an empty prefix (M = 0) PLA is plain causal LA."""
+    q = rnd(1, 2, 33, 16); k = rnd(1, 2, 33, 16); v = rnd(1, 2, 33, 64)
+    ke = np.zeros((1, 2, 0, 16)); ve = np.zeros((1, 2, 0, 64))
+    a = oracle.prefix_prefill(q, k, v, ke, ve)
+    b = oracle.prefill(q, k, v)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_prefix_against_closed_form():
+    """JRT sec. 2.6, Eq. (3) (denominator typo corrected): y_i =
+    phi(q_i)(s_E + s_D,i) / phi(q_i)(z_E + z_D,i), checked against the kernel
+    closed form with the non-causal sum over all M prefix keys."""
+    M, N = 29, 41
+    q = rnd(2, 2, N, 16); k = rnd(2, 2, N, 16); v = rnd(2, 2, N, 16)
+    ke = rnd(2, 2, M, 16); ve = rnd(2, 2, M, 16)
+    y, _, _ = oracle.prefix_prefill(q, k, v, ke, ve)
+    y_ref = quadratic.prefix_closed_form(q, k, v, ke, ve)
+    assert rel(y, y_ref) < 1e-12
+
+
+def test_prefix_self_prefix_full_length():
+    """JRT sec. 2.6: with k_e = k, v_e = v and M = N the prefix sum equals the
+    causal sum at the last position, so y_N(prefix) = y_N(causal)."""
+    N = 45
+    q = rnd(1, 2, N, 16); k = rnd(1, 2, N, 16); v = rnd(1, 2, N, 64)
+    yp, _, _ = oracle.prefix_prefill(q, k, v, k, v)
+    yc, _, _ = oracle.prefill(q, k, v)
+    assert rel(yp[:, :, -1], yc[:, :, -1]) < 1e-13
+
+
+def test_prefix_merge_eq4():
+    """JRT sec. 2.6, Eq. (4): the state after the prefix prefill is
+    s0 + s_E + s_D,N, where s_E is the final state of running the encoder set
+    alone and s_D,N that of the causal set alone."""
+    M, N = 23, 31
+    q = rnd(1, 2, N, 16); k = rnd(1, 2, N, 16); v = rnd(1, 2, N, 64)
+    ke = rnd(1, 2, M, 16); ve = rnd(1, 2, M, 64)
+    s0 = rnd(1, 2, 273, 64); z0 = np.abs(rnd(1, 2, 273)) + 1.0
+    _, s, z = oracle.prefix_prefill(q, k, v, ke, ve, s0, z0)
+    _, sE, zE = oracle.prefill(ke, ke, ve)
+    _, sD, zD = oracle.prefill(q, k, v)
+    assert rel(s, s0 + sE + sD) < 1e-13 and rel(z, z0 + zE + zD) < 1e-13
+
+
+def test_cost_ratio_prefix_vs_causal():
+    """JRT sec. 2.8 / Table 5: JRT-RNN prefill costs about 1.24x Based.  With
+    M = N/2 the prefix only runs the state update (half of the 2*D*(d_v+1)
+    readout + update flops per token), so the algorithmic ratio is 1.25."""
+    D, dv = 273, 64
+    per_token = 2 * D * (dv + 1) * 2       # readout + update
+    per_prefix_token = 2 * D * (dv + 1)   # update only
+    N, M = 32768, 16384
+    ratio = (N * per_token + M * per_prefix_token) / (N * per_token)
+    assert ratio == pytest.approx(1.25)
+    assert per_token == 70980
