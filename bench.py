@@ -1,0 +1,466 @@
+"""Benchmark of the causal Taylor linear-attention hot path on GB300.
+
+One JSON line on stdout (rank 0).  A timed step is one la_prefill call on the
+long-prefill workload (B=16, H=16, N=32768, bf16, non-zero s0/z0 from a
+4096-token prefill); ``value`` is its prefill tokens/s (B*N tokens per step,
+each token covering all 16 heads), summed over ranks.  The same run also
+times the other two calls of the path, reported under ``legs``:
+  - prefix: la_prefix_prefill on the JRT-RNN workload (N=32768, M=16384);
+  - decode: la_decode_step on B=128, H=16, 512 consecutive steps captured in
+    one CUDA graph, state from a 2048-token prefill (tokens/s and HBM GB/s).
+Inputs are seeded synthetic tensors already resident in HBM and larger than
+L2 (2.1 GB of q/k/v per prefill step; the 145 MB decode state is read and
+written every step).  ``e2e`` times the same prefill through the C-ABI with
+pinned host buffers, host->device copies of q, k, v, s0, z0 and
+device->host copies of y, s, z inside the timed region.
+
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no
+collective on the data path); the timed region is bracketed by barriers and
+the max time over ranks is used.
+
+``--impl reference`` times the fp64 CPU oracle (on a bounded sample per
+step) on the same metric, for comparison only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from recurrent_lm_gb300 import inputs  # noqa: E402
+
+METRIC = "prefill tokens/s & % bf16 TC peak (B=16,N=32K); decode tokens/s & % HBM BW"
+FLOPS_PER_HEAD_TOKEN = 70980        # readout 2*273*65 + update 2*273*65
+FLOPS_PER_PREFIX_TOKEN = 35490      # update only
+BYTES_PER_HEAD_TOKEN_BF16 = 320     # q 32 + k 32 + v 128 + y 128
+BYTES_PER_PREFIX_TOKEN_BF16 = 160   # k_e 32 + v_e 128
+STATE_BYTES = 273 * 64 * 4 + 273 * 4  # one head's s and z (fp32)
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------- plumbing
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64,
+                         device=f"cuda:{self.local}" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def done(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if the capture was
+    taken on the current kernel source (profiles/traffic.json records a hash
+    of the source file); None otherwise."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec["bytes_per_launch"] if sha == rec["source_sha"] else None
+
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev: int):
+        self.proc = None
+        self.lines = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(dev).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        mhz, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                mhz.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+def time_loop(fn, steps, warmup, dist):
+    """Run fn() warmup times untimed, then `steps` times between events on the
+    current stream; returns ms per step (max over ranks)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        fn()
+    e1.record(st)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    dist.barrier()
+    return dist.max(e0.elapsed_time(e1) / steps)
+
+
+def gen_device(shape, gen, dtype=torch.bfloat16, dev="cuda"):
+    return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(dtype)
+
+
+# ------------------------------------------------------------------ legs
+def leg_prefill(la, args, dist, dev, clocks):
+    w = inputs.WORKLOADS[3]
+    B, H, N = w.B, w.H, w.N
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 7919 * dist.rank)
+    q = gen_device((B, H, N, 16), g, dev=dev)
+    k = gen_device((B, H, N, 16), g, dev=dev)
+    v = gen_device((B, H, N, 64), g, dev=dev)
+    qs = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
+    ks = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
+    vs = gen_device((B, H, w.s0_tokens, 64), g, dev=dev)
+    _, s0, z0 = la.prefill(qs, ks, vs)
+    del qs, ks, vs
+    y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
+    s = torch.empty_like(s0)
+    z = torch.empty_like(z0)
+
+    def step():
+        la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z)
+
+    clocks.start()
+    ms = time_loop(step, args.steps, args.warmup, dist)
+    clk = clocks.stop()
+    la.check_device_status()
+    out = {"ms": ms, "B": B, "H": H, "N": N, "clocks": clk,
+           "finite": bool(torch.isfinite(y[:, :, -1].float()).all().item())}
+    if not args.no_e2e:
+        out["e2e"] = e2e_prefill(la, args, dist, q, k, v, s0, z0)
+    return out
+
+
+def e2e_prefill(la, args, dist, q, k, v, s0, z0):
+    """Same prefill through the C-ABI from pinned host buffers: H2D of the
+    inputs and D2H of y, s, z inside the timed region."""
+    hq, hk, hv, hs0, hz0 = (t.cpu().pin_memory() for t in (q, k, v, s0, z0))
+    dq, dk, dv_, ds0, dz0 = (torch.empty_like(t) for t in (q, k, v, s0, z0))
+    B, H, N = q.shape[:3]
+    y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=q.device)
+    s = torch.empty_like(s0)
+    z = torch.empty_like(z0)
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    hs = torch.empty(s.shape, dtype=s.dtype).pin_memory()
+    hz = torch.empty(z.shape, dtype=z.dtype).pin_memory()
+
+    def step():
+        for d, h in ((dq, hq), (dk, hk), (dv_, hv), (ds0, hs0), (dz0, hz0)):
+            d.copy_(h, non_blocking=True)
+        la.prefill(dq, dk, dv_, ds0, dz0, y=y, s_out=s, z_out=z)
+        for h, d in ((hy, y), (hs, s), (hz, z)):
+            h.copy_(d, non_blocking=True)
+
+    steps = max(1, min(args.steps, 5))
+    ms = time_loop(step, steps, max(1, min(args.warmup, 2)), dist)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs0, hz0))
+    d2h = sum(t.numel() * t.element_size() for t in (hy, hs, hz))
+    ok = bool(torch.isfinite(hy[:, :, -1].float()).all().item())
+    return {"ms": ms, "steps": steps, "h2d": h2d, "d2h": d2h, "finite": ok}
+
+
+def leg_prefix(la, args, dist, dev):
+    w = inputs.WORKLOADS[4]
+    B, H, N, M = w.B, w.H, w.N, w.M
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 7919 * dist.rank)
+    q = gen_device((B, H, N, 16), g, dev=dev)
+    k = gen_device((B, H, N, 16), g, dev=dev)
+    v = gen_device((B, H, N, 64), g, dev=dev)
+    ke = gen_device((B, H, M, 16), g, dev=dev)
+    ve = gen_device((B, H, M, 64), g, dev=dev)
+    ws = torch.empty(la.prefix_workspace_size(B, H, M), dtype=torch.uint8, device=dev)
+    y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
+    s = torch.empty((B, H, 273, 64), dtype=torch.float32, device=dev)
+    z = torch.empty((B, H, 273), dtype=torch.float32, device=dev)
+
+    def step():
+        la.prefix_prefill(q, k, v, ke, ve, y=y, s_out=s, z_out=z, workspace=ws)
+
+    ms = time_loop(step, max(1, args.steps // 2), max(3, args.warmup // 2), dist)
+    la.check_device_status()
+    return {"ms": ms, "B": B, "H": H, "N": N, "M": M}
+
+
+def leg_decode(la, args, dist, dev):
+    w = inputs.WORKLOADS[5]
+    B, H, T = w.B, w.H, args.decode_steps
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed + 7919 * dist.rank)
+    qs = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
+    ks = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
+    vs = gen_device((B, H, w.s0_tokens, 64), g, dev=dev)
+    _, s, z = la.prefill(qs, ks, vs)
+    del qs, ks, vs
+    qd = gen_device((T, B, H, 16), g, dev=dev)
+    kd = gen_device((T, B, H, 16), g, dev=dev)
+    vd = gen_device((T, B, H, 64), g, dev=dev)
+    yd = torch.empty((T, B, H, 64), dtype=torch.bfloat16, device=dev)
+    # warm up the library (per-device set-up) before capture
+    la.decode_step(qd[0], kd[0], vd[0], s, z, y=yd[0], inplace=True)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(T):
+                la.decode_step(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True)
+    torch.cuda.synchronize()
+    ms = time_loop(graph.replay, max(1, args.steps // 4), max(3, args.warmup // 2), dist)
+    la.check_device_status()
+    ok = bool(torch.isfinite(yd[-1].float()).all().item() and torch.isfinite(s[0, 0]).all().item())
+    return {"ms_per_graph": ms, "steps_per_graph": T, "B": B, "H": H, "finite": ok}
+
+
+def cpu_baseline_prefill(sample_rows: int):
+    """The fp64 oracle, as it stands, on the first `sample_rows` batch rows of
+    the long-prefill workload (all 16 heads, all 32768 tokens, with an s0)."""
+    import oracle
+    w = inputs.WORKLOADS[3]
+    q, k, v, _, _ = inputs.qkv(sample_rows, w.H, w.N, w.seed, w.dtype)
+    s0, z0 = inputs.random_state(sample_rows, w.H, seed=w.seed + 1, tokens=float(w.s0_tokens))
+    t = time.perf_counter()
+    oracle.prefill(q, k, v, s0, z0)
+    dt = time.perf_counter() - t
+    return {"value": sample_rows * w.N / dt, "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{sample_rows} of 16 batch rows x 16 heads x 32768 tokens with s0 "
+                      f"({sample_rows * w.H * w.N} head-tokens, fp64, {dt:.1f} s)"}
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--legs", default="prefill,prefix,decode")
+    ap.add_argument("--decode-steps", type=int, default=512)
+    ap.add_argument("--cpu-sample-rows", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    dist = Dist()
+    if args.impl == "reference":
+        return main_reference(args, dist)
+
+    dist.init("nccl")
+    dev = f"cuda:{dist.local}"
+    torch.cuda.set_device(dev)
+    import recurrent_lm_gb300 as la
+    la.load_library()
+    legs = set(args.legs.split(","))
+    pk = peaks()
+    clocks = Clocks(dist.local)
+
+    pre = leg_prefill(la, args, dist, dev, clocks)
+    res = {}
+    if "prefix" in legs:
+        res["prefix"] = leg_prefix(la, args, dist, dev)
+    if "decode" in legs:
+        res["decode"] = leg_decode(la, args, dist, dev)
+
+    W = dist.world
+    tokens = pre["B"] * pre["N"]
+    head_tokens = pre["B"] * pre["H"] * pre["N"]
+    s_ = pre["ms"] / 1e3
+    flops = head_tokens * FLOPS_PER_HEAD_TOKEN
+    nbytes = head_tokens * BYTES_PER_HEAD_TOKEN_BF16 + 3 * pre["B"] * pre["H"] * STATE_BYTES
+    achieved_tf = flops / s_ / 1e12
+    hbm_gbs = nbytes / s_ / 1e9
+    traffic = kernel_traffic("prefill")
+    line = {
+        "metric": METRIC,
+        "value": W * tokens / s_,
+        "unit": "tokens/s",
+        "n_gpus": W,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": pre["ms"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 tensors resident in HBM)",
+        "config": {"workload": inputs.WORKLOADS[3].name, "B": pre["B"], "H": pre["H"],
+                   "N": pre["N"], "d_feat": 16, "d_v": 64, "D": 273, "s0_tokens": 4096,
+                   "global_batch": W * pre["B"], "seq_len": pre["N"],
+                   "parallelism": f"independent (b,h) shards x{W}",
+                   "l2": "inputs larger than L2 (2.1 GB of q,k,v per step)"},
+        "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16_tflops"],
+                     "traffic": traffic, "peak_source": pk["source"] + " bf16 burst",
+                     "algorithmic_flops_per_launch": flops,
+                     "hbm_achieved_gbs": hbm_gbs, "hbm_peak_gbs": pk["hbm_gbs"],
+                     "hbm_frac": hbm_gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": args.steps,
+        "clocks": pre["clocks"],
+        "legs": {},
+    }
+    if "e2e" in pre:
+        e = pre["e2e"]
+        line["e2e"] = {"value": W * tokens / (e["ms"] / 1e3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                       "ms_per_step": e["ms"], "steps": e["steps"]}
+    launches = args.steps
+    if "prefix" in res:
+        r = res["prefix"]
+        ht = r["B"] * r["H"]
+        fl = ht * (r["N"] * FLOPS_PER_HEAD_TOKEN + r["M"] * FLOPS_PER_PREFIX_TOKEN)
+        by = ht * (r["N"] * BYTES_PER_HEAD_TOKEN_BF16 + r["M"] * BYTES_PER_PREFIX_TOKEN_BF16)
+        t = r["ms"] / 1e3
+        line["legs"]["prefix"] = {
+            "workload": inputs.WORKLOADS[4].name, "ms_per_call": r["ms"],
+            "tokens_per_s": W * r["B"] * r["N"] / t, "achieved_tflops": fl / t / 1e12,
+            "tc_frac": fl / t / 1e12 / pk["bf16_tflops"], "hbm_gbs": by / t / 1e9,
+            "hbm_frac": by / t / 1e9 / pk["hbm_gbs"]}
+        launches += 3 * max(1, args.steps // 2)
+    if "decode" in res:
+        r = res["decode"]
+        per_step_ms = r["ms_per_graph"] / r["steps_per_graph"]
+        bh = r["B"] * r["H"]
+        by = bh * (2 * STATE_BYTES + BYTES_PER_HEAD_TOKEN_BF16)
+        gbs = by / (per_step_ms / 1e3) / 1e9
+        line["legs"]["decode"] = {
+            "workload": inputs.WORKLOADS[5].name, "us_per_step": per_step_ms * 1e3,
+            "tokens_per_s": W * r["B"] / (per_step_ms / 1e3),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "traffic": kernel_traffic("decode"),
+                         "algorithmic_bytes_per_launch": by},
+            "cuda_graph_steps": r["steps_per_graph"], "finite": r["finite"]}
+        launches += r["steps_per_graph"] * max(1, args.steps // 4)
+    line["gpu_launches"] = launches
+    line["gpu_launches_note"] = ("prefill leg: 1 kernel per step; prefix leg: 3 per call; "
+                                 "decode leg: 1 per decode step")
+    line["finite_outputs"] = pre["finite"]
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(args.cpu_sample_rows)
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.done()
+
+
+def main_reference(args, dist):
+    """The fp64 CPU oracle, timed on host cores (rank 0 only)."""
+    if dist.rank != 0:
+        return
+    import oracle
+    w = inputs.WORKLOADS[3]
+    n_sample = 4096
+    q, k, v, _, _ = inputs.qkv(1, w.H, n_sample, w.seed, w.dtype)
+    s0, z0 = inputs.random_state(1, w.H, seed=w.seed + 1, tokens=float(w.s0_tokens))
+    for _ in range(args.warmup):
+        oracle.prefill(q, k, v, s0, z0)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.prefill(q, k, v, s0, z0)
+    dt = (time.perf_counter() - t) / args.steps
+    val = n_sample / dt
+    sample = f"1 of 16 batch rows x 16 heads x {n_sample} of 32768 tokens with s0, per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

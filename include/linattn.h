@@ -1,0 +1,171 @@
+/*
+ * linattn.h -- C ABI of the GB300 (sm_103a) causal Taylor linear-attention
+ * library (liblinattn.so).
+ *
+ * The operation (BASED reading notes, "Simple linear attention language
+ * models balance the recall-throughput tradeoff", sec. 2.2 Eqs. (1)-(3)):
+ *
+ *   s_i = s_{i-1} + phi(k_i) v_i^T      z_i = z_{i-1} + phi(k_i)
+ *   y_i = phi(q_i)^T s_i / (phi(q_i)^T z_i + eps)
+ *
+ * with the second-order Taylor feature map of sec. 2.3 (d' = 16, D = 273):
+ *
+ *   phi(x) = [1, xbar, vec(xbar xbar^T) / sqrt(2)],   xbar = x / d'^(1/4) = x / 2
+ *   phi(q)^T phi(k) = 1 + q.k/4 + (q.k)^2/32
+ *
+ * Feature order in every state buffer: f = 0 constant, f = 1 + a linear,
+ * f = 17 + 16 a + b quadratic (a, b in 0..15).
+ *
+ * Common conventions for every entry point:
+ *  - Every data pointer is a DEVICE pointer to a dense row-major array;
+ *    the caller owns and allocates every buffer.  The library allocates no
+ *    memory and keeps no state between calls (apart from the device status
+ *    word read by la_check_device_status).
+ *  - Activations q, k, v, k_e, v_e and the output y have dtype `dtype`
+ *    (LA_DTYPE_BF16 or LA_DTYPE_F32).  States s, z are always fp32.
+ *    Layouts: q, k [B][H][N][16]; v, y [B][H][N][64]; k_e [B][H][M][16];
+ *    v_e [B][H][M][64]; s [B][H][273][64]; z [B][H][273].
+ *  - Only d_feat = 16 and d_v = 64 are implemented (LA_ERR_UNSUPPORTED else).
+ *  - Every pointer must be 16-byte aligned (LA_ERR_MISALIGNED else).
+ *  - s0 / z0 may be NULL, meaning a zero initial state (both or neither).
+ *    s_out / z_out may be NULL, meaning "do not write the final state".
+ *  - Input and output buffers must not overlap, except that la_decode_step
+ *    accepts s_out == s_in and z_out == z_in exactly (update in place).
+ *  - Work is enqueued on `stream` (NULL = legacy default stream) and runs
+ *    asynchronously.  Argument errors are detected on the host and returned
+ *    before anything is launched; a launch failure returns LA_ERR_CUDA.
+ *  - No exception, abort or process exit ever crosses this boundary.
+ *  - eps is added to the denominator; the pages say an epsilon is added
+ *    without giving its value, and 0 is the default used by every test.
+ */
+#ifndef LINATTN_H_
+#define LINATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LA_API __attribute__((visibility("default")))
+#else
+#define LA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t (a pointer to an opaque
+ * struct), declared here so this header needs no CUDA include. */
+typedef struct CUstream_st *la_stream_t;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,   /* bad shape, NULL required pointer, M > N, overlap */
+    LA_ERR_UNSUPPORTED = 2,   /* d_feat != 16, d_v != 64, unknown dtype, no sm_103 device */
+    LA_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+    LA_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    LA_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (see la_check_device_status) */
+} la_status;
+
+typedef enum {
+    LA_DTYPE_F32 = 0,   /* fp32 activations: CUDA-core fp32 kernels */
+    LA_DTYPE_BF16 = 1   /* bf16 activations: tensor-core kernels, fp32 accumulate */
+} la_dtype;
+
+#define LA_D_FEAT 16
+#define LA_D_V 64
+#define LA_D_PHI 273   /* 1 + 16 + 16*16 */
+
+/*
+ * la_prefill -- causal prefill from an optional initial state.
+ *
+ * Computes y_i for i = 1..N of every (b, h) with the recurrence above,
+ * starting from s0/z0 (state passing: "Understanding and Improving Length
+ * Generalization in Recurrent Models" reading notes, sec. 2.5 Eq. (4) with
+ * the identity transition, so the initial state just adds to the sums), and
+ * writes the final state s_N = s0 + sum_i phi(k_i) v_i^T, z_N likewise.
+ *
+ *   q, k   in   [B][H][N][16] dtype
+ *   v      in   [B][H][N][64] dtype
+ *   s0     in   [B][H][273][64] fp32 or NULL;  z0 in [B][H][273] fp32 or NULL
+ *   y      out  [B][H][N][64] dtype (bf16: rounded to nearest even)
+ *   s_out  out  [B][H][273][64] fp32 or NULL;  z_out out [B][H][273] fp32 or NULL
+ *
+ * B, H >= 1, N >= 0 (N = 0 only copies s0/z0, or zeros, to s_out/z_out).
+ */
+LA_API la_status la_prefill(const void *q, const void *k, const void *v,
+                     const float *s0, const float *z0,
+                     void *y, float *s_out, float *z_out,
+                     int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                     la_dtype dtype, float eps, la_stream_t stream);
+
+/*
+ * la_prefix_workspace_size -- bytes of device scratch la_prefix_prefill
+ * needs for these sizes (0 when M == 0).  The result depends only on
+ * (B, H, M).
+ */
+LA_API size_t la_prefix_workspace_size(int64_t B, int64_t H, int64_t M);
+
+/*
+ * la_prefix_prefill -- JRT-RNN prefix linear attention ("Just read twice"
+ * reading notes, sec. 2.6, Eqs. (3)-(4)).
+ *
+ * A non-causal prefix state is built from a second K/V set over its M
+ * positions,
+ *   s_E = sum_{j<=M} phi(k_e_j) v_e_j^T,   z_E = sum_{j<=M} phi(k_e_j),
+ * and every causal position reads it in addition to the causal state:
+ *   y_i = phi(q_i)(s0 + s_E + s_{D,i}) / (phi(q_i)(z0 + z_E + z_{D,i}) + eps).
+ * The final state is the merge s0 + s_E + s_{D,N} (Eq. (4)).
+ *
+ *   k_e in [B][H][M][16] dtype, v_e in [B][H][M][64] dtype (ignored if M == 0)
+ *   0 <= M <= N, else LA_ERR_INVALID_ARG.
+ *   workspace: device buffer of at least la_prefix_workspace_size(B, H, M)
+ *   bytes, 256-byte aligned, owned by the caller, not read before it is
+ *   written; it may be reused once the call's work on `stream` is done.
+ * Other arguments as for la_prefill.
+ */
+LA_API la_status la_prefix_prefill(const void *q, const void *k, const void *v,
+                            const void *k_e, const void *v_e, int64_t M,
+                            const float *s0, const float *z0,
+                            void *y, float *s_out, float *z_out,
+                            void *workspace, size_t workspace_bytes,
+                            int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                            la_dtype dtype, float eps, la_stream_t stream);
+
+/*
+ * la_decode_step -- one recurrent decode step per (b, h) (BASED reading
+ * notes, sec. 2.2 Eq. (2) for one token; sec. 2.5 notes that decoding still
+ * reads and writes the whole persistent state).  The state is updated first
+ * and then read, so y uses s + phi(k) v^T.
+ *
+ *   q, k   in   [B][H][16] dtype;  v in [B][H][64] dtype
+ *   s_in   in   [B][H][273][64] fp32;  z_in in [B][H][273] fp32 (required)
+ *   s_out  out  [B][H][273][64] fp32;  z_out out [B][H][273] fp32 (required;
+ *               may be exactly s_in / z_in for an in-place update)
+ *   y      out  [B][H][64] dtype
+ */
+LA_API la_status la_decode_step(const void *q, const void *k, const void *v,
+                         const float *s_in, const float *z_in,
+                         float *s_out, float *z_out, void *y,
+                         int64_t B, int64_t H, int d_feat, int d_v,
+                         la_dtype dtype, float eps, la_stream_t stream);
+
+/* Static English description of a status code (never NULL). */
+LA_API const char *la_status_string(la_status status);
+
+/*
+ * la_check_device_status -- synchronizes `stream`, then reads and clears the
+ * library's device status word on the current device.  Returns LA_ERR_TIMEOUT
+ * if any kernel since the last check gave up a bounded wait (its outputs are
+ * then undefined), LA_ERR_CUDA if the synchronization failed, LA_OK else.
+ */
+LA_API la_status la_check_device_status(la_stream_t stream);
+
+/* Library version as major*10000 + minor*100 + patch. */
+LA_API int la_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LINATTN_H_ */

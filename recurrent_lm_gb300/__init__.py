@@ -1,0 +1,11 @@
+"""GB300 (sm_103a) causal Taylor linear attention: prefill, JRT-RNN prefix
+prefill and recurrent decode, computed by the CUDA kernels of liblinattn.so.
+
+The functions below only marshal arguments; see binding.py and
+include/linattn.h.  The seeded workload generators live in ``inputs``.
+"""
+from .binding import (  # noqa: F401
+    D_FEAT, D_PHI, D_V, LA_ERR_CUDA, LA_ERR_INVALID_ARG, LA_ERR_MISALIGNED, LA_ERR_TIMEOUT,
+    LA_ERR_UNSUPPORTED, LA_OK, LAError, LIB_PATH, check_device_status, decode_step,
+    load_library, prefill, prefix_prefill, prefix_workspace_size, status_string,
+)

@@ -1,0 +1,208 @@
+"""Thin Python binding of liblinattn.so (ctypes).
+
+Argument marshalling only: shapes and dtypes are checked, outputs are
+allocated with torch when the caller does not pass them, and every step of the
+computation runs in the library's CUDA kernels on the current torch stream.
+There is no CPU path: calling any function without the built library, or with
+CPU tensors, raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblinattn.so")
+D_FEAT, D_V, D_PHI = 16, 64, 273
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(6)
+LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
+
+_lib = None
+_lock = threading.Lock()
+
+
+class LAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"liblinattn status {status}: {msg}")
+        self.status = status
+
+
+# (name, restype, argtypes) of every symbol declared in include/linattn.h
+_VP, _FP, _I64, _I, _F, _SZ = (ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                               ctypes.c_int, ctypes.c_float, ctypes.c_size_t)
+SIGNATURES = {
+    "la_prefill": (_I, [_VP, _VP, _VP, _FP, _FP, _VP, _FP, _FP, _I64, _I64, _I64, _I, _I,
+                        _I, _F, _VP]),
+    "la_prefix_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "la_prefix_prefill": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _FP, _FP, _VP,
+                               _SZ, _I64, _I64, _I64, _I, _I, _I, _F, _VP]),
+    "la_decode_step": (_I, [_VP, _VP, _VP, _FP, _FP, _FP, _FP, _VP, _I64, _I64, _I, _I, _I,
+                            _F, _VP]),
+    "la_status_string": (ctypes.c_char_p, [_I]),
+    "la_check_device_status": (_I, [_VP]),
+    "la_version": (_I, []),
+}
+
+
+def load_library(path: str = LIB_PATH):
+    """Load liblinattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it first (python -m recurrent_lm_gb300.build); "
+                "there is no fallback implementation")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().la_status_string(int(status)).decode()
+
+
+def _raise(status: int):
+    if status != LA_OK:
+        raise LAError(status, status_string(status))
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return LA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return LA_DTYPE_F32
+    raise TypeError(f"activations must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, shape, dtype):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
+            z_out=None, want_state: bool = True, stream=None):
+    """Causal prefill (la_prefill).  q,k [B,H,N,16], v [B,H,N,64] (bf16 or fp32,
+    CUDA, contiguous); s0 [B,H,273,64], z0 [B,H,273] fp32 or None.
+    Returns (y, s_out, z_out); the states are None when want_state is False."""
+    lib = load_library()
+    B, H, N, _ = q.shape
+    dt = q.dtype
+    _need(q, "q", (B, H, N, D_FEAT), dt)
+    _need(k, "k", (B, H, N, D_FEAT), dt)
+    _need(v, "v", (B, H, N, D_V), dt)
+    if s0 is not None or z0 is not None:
+        _need(s0, "s0", (B, H, D_PHI, D_V), torch.float32)
+        _need(z0, "z0", (B, H, D_PHI), torch.float32)
+    if y is None:
+        y = torch.empty((B, H, N, D_V), dtype=dt, device=q.device)
+    _need(y, "y", (B, H, N, D_V), dt)
+    if want_state:
+        if s_out is None:
+            s_out = torch.empty((B, H, D_PHI, D_V), dtype=torch.float32, device=q.device)
+        if z_out is None:
+            z_out = torch.empty((B, H, D_PHI), dtype=torch.float32, device=q.device)
+    if s_out is not None:
+        _need(s_out, "s_out", (B, H, D_PHI, D_V), torch.float32)
+    if z_out is not None:
+        _need(z_out, "z_out", (B, H, D_PHI), torch.float32)
+    _raise(lib.la_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
+                          _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q), float(eps), _stream(stream)))
+    return y, s_out, z_out
+
+
+def prefix_workspace_size(B: int, H: int, M: int) -> int:
+    return int(load_library().la_prefix_workspace_size(B, H, M))
+
+
+def prefix_prefill(q, k, v, k_e, v_e, s0=None, z0=None, *, eps: float = 0.0, y=None,
+                   s_out=None, z_out=None, want_state: bool = True, workspace=None,
+                   stream=None):
+    """JRT-RNN prefix linear attention (la_prefix_prefill).  k_e [B,H,M,16],
+    v_e [B,H,M,64] with M <= N.  ``workspace`` is a CUDA uint8 tensor of at
+    least prefix_workspace_size(B, H, M) bytes (allocated here if None)."""
+    lib = load_library()
+    B, H, N, _ = q.shape
+    dt = q.dtype
+    M = k_e.shape[2]
+    _need(q, "q", (B, H, N, D_FEAT), dt)
+    _need(k, "k", (B, H, N, D_FEAT), dt)
+    _need(v, "v", (B, H, N, D_V), dt)
+    _need(k_e, "k_e", (B, H, M, D_FEAT), dt)
+    _need(v_e, "v_e", (B, H, M, D_V), dt)
+    if s0 is not None or z0 is not None:
+        _need(s0, "s0", (B, H, D_PHI, D_V), torch.float32)
+        _need(z0, "z0", (B, H, D_PHI), torch.float32)
+    if y is None:
+        y = torch.empty((B, H, N, D_V), dtype=dt, device=q.device)
+    if want_state:
+        if s_out is None:
+            s_out = torch.empty((B, H, D_PHI, D_V), dtype=torch.float32, device=q.device)
+        if z_out is None:
+            z_out = torch.empty((B, H, D_PHI), dtype=torch.float32, device=q.device)
+    need = prefix_workspace_size(B, H, M)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _raise(lib.la_prefix_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_e), _ptr(v_e), M, _ptr(s0), _ptr(z0), _ptr(y),
+        _ptr(s_out), _ptr(z_out), _ptr(workspace), workspace.numel(), B, H, N, D_FEAT, D_V,
+        _dt(q), float(eps), _stream(stream)))
+    return y, s_out, z_out
+
+
+def decode_step(q, k, v, s, z, *, eps: float = 0.0, y=None, s_out=None, z_out=None,
+                inplace: bool = False, stream=None):
+    """One decode step (la_decode_step).  q,k [B,H,16], v [B,H,64]; s [B,H,273,64],
+    z [B,H,273] fp32.  With inplace=True the state is updated in s, z."""
+    lib = load_library()
+    B, H, _ = q.shape
+    dt = q.dtype
+    _need(q, "q", (B, H, D_FEAT), dt)
+    _need(k, "k", (B, H, D_FEAT), dt)
+    _need(v, "v", (B, H, D_V), dt)
+    _need(s, "s", (B, H, D_PHI, D_V), torch.float32)
+    _need(z, "z", (B, H, D_PHI), torch.float32)
+    if inplace:
+        s_out, z_out = s, z
+    if s_out is None:
+        s_out = torch.empty_like(s)
+    if z_out is None:
+        z_out = torch.empty_like(z)
+    if y is None:
+        y = torch.empty((B, H, D_V), dtype=dt, device=q.device)
+    _raise(lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(z), _ptr(s_out),
+                              _ptr(z_out), _ptr(y), B, H, D_FEAT, D_V, _dt(q), float(eps),
+                              _stream(stream)))
+    return y, s_out, z_out
+
+
+def check_device_status(stream=None) -> None:
+    """Synchronize and raise LAError(LA_ERR_TIMEOUT) if a bounded wait gave up."""
+    _raise(load_library().la_check_device_status(_stream(stream)))

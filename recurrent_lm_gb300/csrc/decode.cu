@@ -1,0 +1,140 @@
+// Recurrent decode step: one token per (b, h), bandwidth bound.
+//
+// BASED reading notes ("Simple linear attention language models balance the
+// recall-throughput tradeoff"), sec. 2.2 Eq. (2) for a single token, and
+// sec. 2.5: the decode kernel fuses the outer-product write with the query
+// read-out but still reads and writes the whole persistent state.
+//
+// Per head the state is s [273][64] fp32 (69,888 B) + z [273] fp32; one CTA
+// streams it once: every thread owns one float4 column group (16 per row) of
+// a strided set of rows, issues all of its row loads before using any (so a
+// CTA keeps ~70 KB in flight), applies s += phi(k)_r v, writes the row back
+// and accumulates phi(q)_r * s_r for the numerator.  Partial numerators are
+// summed across the 16 row groups in shared memory; the normaliser phi(q).z
+// uses a warp-shuffle reduction.
+#include "la_device.cuh"
+#include "la_internal.h"
+
+namespace la {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kColGroups = kDV / 4;              // 16 float4 per state row
+constexpr int kRowGroups = kThreads / kColGroups;  // 16
+constexpr int kRowsPerThread = (kD + kRowGroups - 1) / kRowGroups;  // 18
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2)
+decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
+                   const T *__restrict__ v, const float *s_in, const float *z_in,
+                   float *s_out, float *z_out, T *__restrict__ y, float eps) {
+    __shared__ float xq[kDFeat], xk[kDFeat];
+    __shared__ float phq[kD + 15], phk[kD + 15];
+    __shared__ float4 red[kRowGroups][kColGroups];
+    __shared__ float den_part[kThreads / 32];
+
+    const int64_t bh = blockIdx.x;
+    const int tid = threadIdx.x;
+    if (tid < kDFeat) xq[tid] = 0.5f * Act<T>::load(q, bh * kDFeat + tid);
+    else if (tid < 2 * kDFeat) xk[tid - kDFeat] = 0.5f * Act<T>::load(k, bh * kDFeat + tid - kDFeat);
+
+    const int cg = tid % kColGroups;   // float4 column group
+    const int rg = tid / kColGroups;   // row group: rows rg, rg + 16, ...
+    const float4 *src = reinterpret_cast<const float4 *>(s_in + bh * (int64_t)kD * kDV);
+    float4 *dst = reinterpret_cast<float4 *>(s_out + bh * (int64_t)kD * kDV);
+
+    // Issue every state load of this thread up front.
+    float4 sr[kRowsPerThread];
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; ++j) {
+        const int r = rg + j * kRowGroups;
+        if (r < kD) sr[j] = src[r * kColGroups + cg];
+    }
+    const float zin0 = z_in[bh * kD + tid];
+    const float zin1 = (tid + kThreads < kD) ? z_in[bh * kD + tid + kThreads] : 0.f;
+    float4 vv;
+    vv.x = Act<T>::load(v, bh * kDV + cg * 4 + 0);
+    vv.y = Act<T>::load(v, bh * kDV + cg * 4 + 1);
+    vv.z = Act<T>::load(v, bh * kDV + cg * 4 + 2);
+    vv.w = Act<T>::load(v, bh * kDV + cg * 4 + 3);
+    __syncthreads();
+
+    for (int f = tid; f < kD; f += kThreads) {
+        phq[f] = phi_feature(xq, f);
+        phk[f] = phi_feature(xk, f);
+    }
+    __syncthreads();
+
+    // z update and the normaliser phi(q).z_new.
+    float dpart = 0.f;
+    {
+        const float zn = zin0 + phk[tid];
+        z_out[bh * kD + tid] = zn;
+        dpart = phq[tid] * zn;
+        if (tid + kThreads < kD) {
+            const int f = tid + kThreads;
+            const float zn1 = zin1 + phk[f];
+            z_out[bh * kD + f] = zn1;
+            dpart += phq[f] * zn1;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dpart += __shfl_xor_sync(0xffffffffu, dpart, o);
+    if ((tid & 31) == 0) den_part[tid >> 5] = dpart;
+
+    // s update (write back) and the numerator partials.
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; ++j) {
+        const int r = rg + j * kRowGroups;
+        if (r < kD) {
+            const float pk = phk[r], pq = phq[r];
+            float4 s = sr[j];
+            s.x = fmaf(pk, vv.x, s.x);
+            s.y = fmaf(pk, vv.y, s.y);
+            s.z = fmaf(pk, vv.z, s.z);
+            s.w = fmaf(pk, vv.w, s.w);
+            dst[r * kColGroups + cg] = s;
+            acc.x = fmaf(pq, s.x, acc.x);
+            acc.y = fmaf(pq, s.y, acc.y);
+            acc.z = fmaf(pq, s.z, acc.z);
+            acc.w = fmaf(pq, s.w, acc.w);
+        }
+    }
+    red[rg][cg] = acc;
+    __syncthreads();
+
+    if (tid < kDV) {
+        float den = eps;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) den += den_part[w];
+        const int c4 = tid >> 2, lane4 = tid & 3;
+        float num = 0.f;
+#pragma unroll
+        for (int g = 0; g < kRowGroups; ++g) {
+            const float4 p = red[g][c4];
+            num += lane4 == 0 ? p.x : lane4 == 1 ? p.y : lane4 == 2 ? p.z : p.w;
+        }
+        Act<T>::store(y, bh * kDV + tid, num / den);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, la_dtype dt, cudaStream_t st) {
+    const int64_t BH = a.B * a.H;
+    if (BH == 0) return cudaSuccess;
+    dim3 grid((unsigned)BH), block(kThreads);
+    if (dt == LA_DTYPE_BF16)
+        decode_step_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(
+            (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k,
+            (const __nv_bfloat16 *)a.v, a.s_in, a.z_in, a.s_out, a.z_out,
+            (__nv_bfloat16 *)a.y, a.eps);
+    else
+        decode_step_kernel<float><<<grid, block, 0, st>>>(
+            (const float *)a.q, (const float *)a.k, (const float *)a.v, a.s_in,
+            a.z_in, a.s_out, a.z_out, (float *)a.y, a.eps);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -1,0 +1,261 @@
+// C-ABI layer of liblinattn.so: argument validation on the host, workspace
+// carving, and dispatch to the kernel launchers.  Nothing is launched unless
+// every argument check passes.  See include/linattn.h for the contract.
+#include <mutex>
+
+#include "la_internal.h"
+
+namespace {
+
+using la::kD;
+using la::kDV;
+using la::kDFeat;
+
+__device__ unsigned g_la_status = 0;
+
+constexpr int kMaxDevices = 64;
+unsigned *g_status_ptr[kMaxDevices] = {};
+int g_cc[kMaxDevices] = {};  // major*10+minor, 0 = not queried yet
+std::mutex g_mu;
+
+// Per-device set-up: compute capability and the status word's address.
+la_status device_setup(int *dev_out, unsigned **status) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_cc[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return LA_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_la_status) != cudaSuccess) return LA_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<unsigned *>(p);
+        g_cc[dev] = major * 10 + minor;
+    }
+    if (g_cc[dev] != 103) return LA_ERR_UNSUPPORTED;  // kernels are built for sm_103a only
+    *dev_out = dev;
+    *status = g_status_ptr[dev];
+    return LA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    const void *p;
+    size_t bytes;
+};
+
+bool overlaps(Range a, Range b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Checks that no output range overlaps any input range or another output.
+bool any_overlap(const Range *in, int nin, const Range *out, int nout) {
+    for (int i = 0; i < nout; ++i) {
+        for (int j = 0; j < nin; ++j)
+            if (overlaps(out[i], in[j])) return true;
+        for (int j = i + 1; j < nout; ++j)
+            if (overlaps(out[i], out[j])) return true;
+    }
+    return false;
+}
+
+// Shape limits: every grid dimension used is (B*H) or segments; element
+// counts are 64-bit everywhere in the kernels.
+constexpr int64_t kMaxBH = (int64_t(1) << 31) - 1;
+constexpr int64_t kMaxTokens = int64_t(1) << 40;
+
+la_status check_common(int64_t B, int64_t H, int64_t N, int d_feat, int d_v, la_dtype dtype) {
+    if (d_feat != kDFeat || d_v != kDV) return LA_ERR_UNSUPPORTED;
+    if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
+    if (B < 1 || H < 1 || N < 0) return LA_ERR_INVALID_ARG;
+    if (B > kMaxBH / H) return LA_ERR_INVALID_ARG;
+    if (N > kMaxTokens / (B * H)) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+size_t esize(la_dtype dt) { return dt == LA_DTYPE_BF16 ? 2 : 4; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct PrefixLayout {
+    size_t part_s, part_z, s_init, z_init, total;
+};
+
+PrefixLayout prefix_layout(int64_t BH, int64_t M) {
+    PrefixLayout L{};
+    if (M <= 0) return L;
+    const int64_t nseg = la::prefix_nseg(M);
+    size_t off = 0;
+    L.part_s = off; off = align256(off + sizeof(float) * BH * nseg * kD * kDV);
+    L.part_z = off; off = align256(off + sizeof(float) * BH * nseg * kD);
+    L.s_init = off; off = align256(off + sizeof(float) * BH * kD * kDV);
+    L.z_init = off; off = align256(off + sizeof(float) * BH * kD);
+    L.total = off;
+    return L;
+}
+
+cudaError_t run_prefill(const la::PrefillArgs &a, la_dtype dtype, cudaStream_t st) {
+    const int64_t BH = a.B * a.H;
+    if (a.N == 0) {
+        if (!a.s_out && !a.z_out) return cudaSuccess;
+        return la::launch_state_copy(a.s0, a.z0, a.s_out, a.z_out, BH, st);
+    }
+    return la::launch_prefill_simt(a, dtype, st);
+}
+
+la_status to_status(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int la_version(void) { return 100; }
+
+const char *la_status_string(la_status s) {
+    switch (s) {
+        case LA_OK: return "ok";
+        case LA_ERR_INVALID_ARG: return "invalid argument (shape, NULL pointer, M > N or overlapping buffers)";
+        case LA_ERR_UNSUPPORTED: return "unsupported (d_feat must be 16, d_v 64, dtype f32/bf16, device sm_103)";
+        case LA_ERR_MISALIGNED: return "a buffer is not 16-byte aligned";
+        case LA_ERR_CUDA: return "CUDA runtime error or kernel launch failure";
+        case LA_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    }
+    return "unknown status";
+}
+
+la_status la_prefill(const void *q, const void *k, const void *v, const float *s0,
+                     const float *z0, void *y, float *s_out, float *z_out, int64_t B,
+                     int64_t H, int64_t N, int d_feat, int d_v, la_dtype dtype, float eps,
+                     la_stream_t stream) {
+    la_status st = check_common(B, H, N, d_feat, d_v, dtype);
+    if (st != LA_OK) return st;
+    if ((s0 == nullptr) != (z0 == nullptr)) return LA_ERR_INVALID_ARG;
+    if (N > 0 && (!q || !k || !v || !y)) return LA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, s0, z0, y, s_out, z_out};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
+    const int64_t BH = B * H;
+    const size_t es = esize(dtype);
+    const Range in[] = {{q, es * BH * N * kDFeat}, {k, es * BH * N * kDFeat},
+                        {v, es * BH * N * kDV}, {s0, sizeof(float) * BH * kD * kDV},
+                        {z0, sizeof(float) * BH * kD}};
+    const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * kD * kDV},
+                         {z_out, sizeof(float) * BH * kD}};
+    if (any_overlap(in, 5, out, 3)) return LA_ERR_INVALID_ARG;
+    int dev;
+    unsigned *status;
+    if ((st = device_setup(&dev, &status)) != LA_OK) return st;
+    la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status};
+    return to_status(run_prefill(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t la_prefix_workspace_size(int64_t B, int64_t H, int64_t M) {
+    if (B < 1 || H < 1 || M <= 0 || B > kMaxBH / H) return 0;
+    return prefix_layout(B * H, M).total;
+}
+
+la_status la_prefix_prefill(const void *q, const void *k, const void *v, const void *k_e,
+                            const void *v_e, int64_t M, const float *s0, const float *z0,
+                            void *y, float *s_out, float *z_out, void *workspace,
+                            size_t workspace_bytes, int64_t B, int64_t H, int64_t N,
+                            int d_feat, int d_v, la_dtype dtype, float eps,
+                            la_stream_t stream) {
+    la_status st = check_common(B, H, N, d_feat, d_v, dtype);
+    if (st != LA_OK) return st;
+    if (M < 0 || M > N) return LA_ERR_INVALID_ARG;
+    if (M == 0)
+        return la_prefill(q, k, v, s0, z0, y, s_out, z_out, B, H, N, d_feat, d_v, dtype,
+                          eps, stream);
+    if ((s0 == nullptr) != (z0 == nullptr)) return LA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !y || !k_e || !v_e || !workspace) return LA_ERR_INVALID_ARG;
+    const int64_t BH = B * H;
+    const PrefixLayout L = prefix_layout(BH, M);
+    if (workspace_bytes < L.total) return LA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, k_e, v_e, s0, z0, y, s_out, z_out};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LA_ERR_MISALIGNED;
+    const size_t es = esize(dtype);
+    const Range in[] = {{q, es * BH * N * kDFeat}, {k, es * BH * N * kDFeat},
+                        {v, es * BH * N * kDV}, {k_e, es * BH * M * kDFeat},
+                        {v_e, es * BH * M * kDV}, {s0, sizeof(float) * BH * kD * kDV},
+                        {z0, sizeof(float) * BH * kD}};
+    const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * kD * kDV},
+                         {z_out, sizeof(float) * BH * kD}, {workspace, L.total}};
+    if (any_overlap(in, 7, out, 4)) return LA_ERR_INVALID_ARG;
+    int dev;
+    unsigned *status;
+    if ((st = device_setup(&dev, &status)) != LA_OK) return st;
+
+    char *ws = static_cast<char *>(workspace);
+    la::PrefixArgs pa{};
+    pa.k_e = k_e; pa.v_e = v_e; pa.B = B; pa.H = H; pa.M = M;
+    pa.seg_len = la::kPrefixSeg; pa.nseg = la::prefix_nseg(M);
+    pa.part_s = reinterpret_cast<float *>(ws + L.part_s);
+    pa.part_z = reinterpret_cast<float *>(ws + L.part_z);
+    pa.s0 = s0; pa.z0 = z0;
+    pa.s_init = reinterpret_cast<float *>(ws + L.s_init);
+    pa.z_init = reinterpret_cast<float *>(ws + L.z_init);
+    pa.status = status;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = la::launch_prefix_partials_simt(pa, dtype, cs);
+    if (e == cudaSuccess) e = la::launch_prefix_reduce(pa, cs);
+    if (e != cudaSuccess) return LA_ERR_CUDA;
+    la::PrefillArgs a{q, k, v, pa.s_init, pa.z_init, y, s_out, z_out, B, H, N, eps, status};
+    return to_status(run_prefill(a, dtype, cs));
+}
+
+la_status la_decode_step(const void *q, const void *k, const void *v, const float *s_in,
+                         const float *z_in, float *s_out, float *z_out, void *y, int64_t B,
+                         int64_t H, int d_feat, int d_v, la_dtype dtype, float eps,
+                         la_stream_t stream) {
+    la_status st = check_common(B, H, 1, d_feat, d_v, dtype);
+    if (st != LA_OK) return st;
+    if (!q || !k || !v || !s_in || !z_in || !s_out || !z_out || !y) return LA_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, s_in, z_in, s_out, z_out, y};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return LA_ERR_MISALIGNED;
+    const int64_t BH = B * H;
+    const size_t es = esize(dtype);
+    const size_t sb = sizeof(float) * BH * kD * kDV, zb = sizeof(float) * BH * kD;
+    // exact aliasing s_out == s_in / z_out == z_in is the in-place update
+    const Range in[] = {{q, es * BH * kDFeat}, {k, es * BH * kDFeat}, {v, es * BH * kDV},
+                        {s_out == s_in ? nullptr : s_in, sb},
+                        {z_out == z_in ? nullptr : z_in, zb}};
+    const Range out[] = {{y, es * BH * kDV}, {s_out, sb}, {z_out, zb}};
+    if (any_overlap(in, 5, out, 3)) return LA_ERR_INVALID_ARG;
+    // an in-place state must not overlap the other state buffer or y either
+    if (s_out == s_in && (overlaps({s_in, sb}, {z_in, zb}) || overlaps({s_in, sb}, {y, es * BH * kDV})))
+        return LA_ERR_INVALID_ARG;
+    int dev;
+    unsigned *status;
+    if ((st = device_setup(&dev, &status)) != LA_OK) return st;
+    la::DecodeArgs a{q, k, v, s_in, z_in, s_out, z_out, y, B, H, eps};
+    return to_status(la::launch_decode(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+la_status la_check_device_status(la_stream_t stream) {
+    int dev;
+    unsigned *status;
+    la_status st = device_setup(&dev, &status);
+    if (st != LA_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return LA_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LA_ERR_CUDA;
+    if (word != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return LA_ERR_CUDA;
+        return LA_ERR_TIMEOUT;
+    }
+    return LA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal interface between the C-ABI layer (la_api.cu) and the kernel
+// translation units.  Launchers assume their arguments were validated by the
+// ABI layer and return the cudaError_t of the launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "linattn.h"
+
+namespace la {
+
+constexpr int kDFeat = 16;     // d'
+constexpr int kDV = 64;        // d_v
+constexpr int kD = 273;        // 1 + d' + d'^2
+constexpr int kStateFloats = kD * kDV + kD;  // one head's s and z
+
+// Bits of the device status word (one per failure class).
+constexpr unsigned kStatusTimeout = 1u;
+
+struct PrefillArgs {
+    const void *q, *k, *v;
+    const float *s0, *z0;
+    void *y;
+    float *s_out, *z_out;
+    int64_t B, H, N;
+    float eps;
+    unsigned *status;   // device status word
+};
+
+struct DecodeArgs {
+    const void *q, *k, *v;
+    const float *s_in, *z_in;
+    float *s_out, *z_out;
+    void *y;
+    int64_t B, H;
+    float eps;
+};
+
+// Per-segment partial prefix states: part_s [BH][nseg][273][64],
+// part_z [BH][nseg][273] (fp32), reduced into s0' / z0'.
+struct PrefixArgs {
+    const void *k_e, *v_e;
+    int64_t B, H, M;
+    int64_t seg_len, nseg;
+    float *part_s, *part_z;
+    const float *s0, *z0;
+    float *s_init, *z_init;   // s0 + s_E, z0 + z_E  [BH][273][64], [BH][273]
+    unsigned *status;
+};
+
+// Token-segment length of the prefix reduction and its workspace layout.
+constexpr int64_t kPrefixSeg = 2048;
+inline int64_t prefix_nseg(int64_t M) { return (M + kPrefixSeg - 1) / kPrefixSeg; }
+
+cudaError_t launch_decode(const DecodeArgs &a, la_dtype dt, cudaStream_t st);
+cudaError_t launch_prefill_simt(const PrefillArgs &a, la_dtype dt, cudaStream_t st);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st);
+cudaError_t launch_prefix_partials_simt(const PrefixArgs &a, la_dtype dt, cudaStream_t st);
+cudaError_t launch_prefix_partials_tc(const PrefixArgs &a, cudaStream_t st);
+cudaError_t launch_prefix_reduce(const PrefixArgs &a, cudaStream_t st);
+cudaError_t launch_state_copy(const float *s0, const float *z0, float *s_out,
+                              float *z_out, int64_t BH, cudaStream_t st);
+
+}  // namespace la

@@ -1,0 +1,158 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/*.h declares, and rejects bad arguments on the host before
+any CUDA call (fake, never-dereferenced pointer values are used for that)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from recurrent_lm_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names |= set(re.findall(r"LA_API\s+[\w\s\*]*?\b(la_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    assert {"la_prefill", "la_prefix_prefill", "la_decode_step"} <= names
+    assert len(names) >= 6
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in binding.SIGNATURES, f"binding has no signature for {name}"
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert binding.status_string(s)
+    assert "unknown" in binding.status_string(99)
+    assert lib.la_version() >= 100
+
+
+# Fake device addresses: 16-byte aligned, far apart, never dereferenced
+# because every call below fails validation before touching the device.
+A = 0x7f0000000000
+STEP = 1 << 36
+
+
+def fake(i, misalign=0):
+    return ctypes.c_void_p(A + i * STEP + misalign)
+
+
+def call_prefill(lib, B=1, H=1, N=8, dk=16, dv=64, dtype=1, ptrs=None, s0=True):
+    p = ptrs or [fake(i) for i in range(8)]
+    if not s0:
+        p[3] = None
+        p[4] = None
+    return lib.la_prefill(*p, B, H, N, dk, dv, dtype, 0.0, None)
+
+
+def test_prefill_rejects_unsupported_dims(lib):
+    assert call_prefill(lib, dk=8) == binding.LA_ERR_UNSUPPORTED
+    assert call_prefill(lib, dv=32) == binding.LA_ERR_UNSUPPORTED
+    assert call_prefill(lib, dtype=7) == binding.LA_ERR_UNSUPPORTED
+
+
+def test_prefill_rejects_bad_shapes(lib):
+    assert call_prefill(lib, B=0) == binding.LA_ERR_INVALID_ARG
+    assert call_prefill(lib, H=-1) == binding.LA_ERR_INVALID_ARG
+    assert call_prefill(lib, N=-5) == binding.LA_ERR_INVALID_ARG
+    assert call_prefill(lib, B=1 << 20, H=1 << 20) == binding.LA_ERR_INVALID_ARG
+
+
+def test_prefill_rejects_null_and_half_state(lib):
+    p = [fake(i) for i in range(8)]
+    p[0] = None  # q
+    assert call_prefill(lib, ptrs=p) == binding.LA_ERR_INVALID_ARG
+    p = [fake(i) for i in range(8)]
+    p[4] = None  # z0 without s0
+    assert call_prefill(lib, ptrs=p) == binding.LA_ERR_INVALID_ARG
+
+
+def test_prefill_rejects_misaligned(lib):
+    for i in range(8):
+        p = [fake(j) for j in range(8)]
+        p[i] = fake(i, misalign=4)
+        assert call_prefill(lib, ptrs=p) == binding.LA_ERR_MISALIGNED, i
+
+
+def test_prefill_rejects_overlap(lib):
+    p = [fake(i) for i in range(8)]
+    p[5] = ctypes.c_void_p(p[2].value + 64)  # y inside v
+    assert call_prefill(lib, ptrs=p) == binding.LA_ERR_INVALID_ARG
+    p = [fake(i) for i in range(8)]
+    p[6] = ctypes.c_void_p(p[3].value)       # s_out == s0 (prefill is not in place)
+    assert call_prefill(lib, ptrs=p) == binding.LA_ERR_INVALID_ARG
+
+
+def test_prefix_rejects_m_greater_than_n(lib):
+    p = [fake(i) for i in range(12)]
+    rc = lib.la_prefix_prefill(p[0], p[1], p[2], p[3], p[4], 9, p[5], p[6], p[7], p[8], p[9],
+                               p[10], 1 << 40, 1, 1, 8, 16, 64, 1, 0.0, None)
+    assert rc == binding.LA_ERR_INVALID_ARG
+    rc = lib.la_prefix_prefill(p[0], p[1], p[2], p[3], p[4], -1, p[5], p[6], p[7], p[8], p[9],
+                               p[10], 1 << 40, 1, 1, 8, 16, 64, 1, 0.0, None)
+    assert rc == binding.LA_ERR_INVALID_ARG
+
+
+def test_prefix_rejects_small_or_misaligned_workspace(lib):
+    need = lib.la_prefix_workspace_size(2, 3, 5000)
+    assert need > 0 and need % 256 == 0
+    assert lib.la_prefix_workspace_size(2, 3, 0) == 0
+    p = [fake(i) for i in range(12)]
+    rc = lib.la_prefix_prefill(p[0], p[1], p[2], p[3], p[4], 5000, p[5], p[6], p[7], p[8], p[9],
+                               p[10], need - 1, 2, 3, 8000, 16, 64, 1, 0.0, None)
+    assert rc == binding.LA_ERR_INVALID_ARG
+    ws = ctypes.c_void_p(p[10].value + 16)   # 16- but not 256-byte aligned
+    rc = lib.la_prefix_prefill(p[0], p[1], p[2], p[3], p[4], 5000, p[5], p[6], p[7], p[8], p[9],
+                               ws, need, 2, 3, 8000, 16, 64, 1, 0.0, None)
+    assert rc == binding.LA_ERR_MISALIGNED
+
+
+def test_decode_rejects_bad_args(lib):
+    p = [fake(i) for i in range(8)]
+    assert lib.la_decode_step(*p, 4, 2, 16, 32, 1, 0.0, None) == binding.LA_ERR_UNSUPPORTED
+    assert lib.la_decode_step(*p, 0, 2, 16, 64, 1, 0.0, None) == binding.LA_ERR_INVALID_ARG
+    q = list(p); q[3] = None
+    assert lib.la_decode_step(*q, 4, 2, 16, 64, 1, 0.0, None) == binding.LA_ERR_INVALID_ARG
+    q = list(p); q[7] = fake(7, misalign=8)
+    assert lib.la_decode_step(*q, 4, 2, 16, 64, 1, 0.0, None) == binding.LA_ERR_MISALIGNED
+    q = list(p); q[5] = ctypes.c_void_p(p[3].value + 256)   # s_out partially overlaps s_in
+    assert lib.la_decode_step(*q, 4, 2, 16, 64, 1, 0.0, None) == binding.LA_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 1, 4, 16, dtype=torch.bfloat16)
+    v = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.prefill(q, q, v)
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    mod = importlib.import_module("recurrent_lm_gb300.binding")
+    saved = mod._lib
+    try:
+        mod._lib = None
+        with pytest.raises(RuntimeError, match="missing"):
+            mod.load_library(str(tmp_path / "nope.so"))
+    finally:
+        mod._lib = saved
