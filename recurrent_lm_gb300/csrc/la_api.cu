@@ -105,6 +105,7 @@ cudaError_t run_prefill(const la::PrefillArgs &a, la_dtype dtype, cudaStream_t s
         if (!a.s_out && !a.z_out) return cudaSuccess;
         return la::launch_state_copy(a.s0, a.z0, a.s_out, a.z_out, BH, st);
     }
+    if (dtype == LA_DTYPE_BF16) return la::launch_prefill_tc(a, st);
     return la::launch_prefill_simt(a, dtype, st);
 }
 
