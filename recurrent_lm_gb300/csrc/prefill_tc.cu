@@ -12,22 +12,26 @@
 // GB300 design (one CTA per (b, h), 512 threads, 1 CTA per SM):
 //  * Intra-chunk term without feature vectors: T = Q K^T on the tensor core
 //    (K = 16), then P = 1 + T/4 + T^2/32 (the Taylor kernel, BASED sec. 2.3)
-//    with the causal mask in registers, then P V and P 1 on the tensor core.
-//  * Inter-chunk terms on the tensor core with a symmetric-compact feature
-//    map inside the kernel: 136 quadratic features (a <= b) + 1 + 16 + 7 pad
-//    = 160 instead of 273 (BASED sec. 2.3 table: 1 + d' + d'(d'+1)/2 = 153).
-//    Query features carry xbar_a xbar_b, key features xbar_a xbar_b (a < b)
-//    and xbar_a^2 / 2, so Phi'_Q . Phi'_K = 1 + q.k/4 + (q.k)^2/32 exactly.
-//    The state is held as S' (160 x 64 fp32 in TMEM); it is converted from /
-//    to the 273-row layout of the C ABI at the start / end (the antisymmetric
-//    part of a caller's s0 cannot influence any output and is passed through).
-//  * The normaliser rides on the same MMAs with N = 16 operands: z' via a
-//    ones matrix (z' += Phi'_K^T 1), and den via Phi'_Q z' and P 1.
+//    with the causal mask in registers, written back in place into TMEM as
+//    bf16, then [num | den] = P [V | 1] with P as the TMEM A operand.
+//  * Inter-chunk terms with a symmetric-compact feature map inside the
+//    kernel: 136 quadratic features (a <= b) + 1 + 16 + 7 pad = 160 instead
+//    of 273 (BASED sec. 2.3 table: 1 + d' + d'(d'+1)/2 = 153).  Query features
+//    carry xbar_a xbar_b, key features xbar_a xbar_b (a < b) and xbar_a^2 / 2,
+//    so Phi'_Q . Phi'_K = 1 + q.k/4 + (q.k)^2/32 exactly.
+//  * The state is kept transposed, S'^T (values x features, fp32 in TMEM),
+//    and updated as [S'^T ; z'] += [V | 1]^T Phi'_K: one M = 128, N = 160 MMA
+//    per 16 tokens (the 64 value rows plus ones rows that yield z').  Its
+//    bf16 copy is then directly the K-major B operand of the read-out
+//    [num | den] += Phi'_Q [S' | z'].  The 273-row C-ABI state is converted
+//    at the start and the end (the antisymmetric part of a caller's s0 cannot
+//    influence any output and is passed through unchanged).
+//  * These MMAs have small N and are bound by shared-memory operand
+//    bandwidth, so the layout minimises operand bytes per chunk.
 //  * Roles: warp 0 TMA producer (q, k, v chunks, zero-filled past N), warp 1
 //    MMA issuer, warpgroup 1 feature generation (one token per thread),
-//    warpgroup 2 P epilogue and output epilogue y = num / den, warpgroup 3
-//    state conversion S' (TMEM, fp32) -> bf16 shared-memory operand for the
-//    next chunk's read-out, and the final state store.
+//    warpgroup 2 P epilogue, warpgroup 3 output epilogue y = num / den and
+//    the state conversion (TMEM fp32 -> bf16 operand, final state store).
 //  * Every wait is bounded: after ~1 s the kernel records a timeout in the
 //    device status word and every role unwinds.
 #include <utility>
@@ -42,28 +46,26 @@ using namespace tc;
 
 constexpr int kC = 128;          // tokens per chunk
 constexpr int kThreads = 512;
-constexpr int kNQuad = 136;      // a <= b pairs
-constexpr int kFConst = 136;
-constexpr int kFLin = 137;
-constexpr int kNReal = 153;
+constexpr int kNFeat = 160;      // compact features (153 real + 7 zero)
+constexpr int kNB = 80;          // B columns of the value side: 64 values + 16 normaliser
 
-// TMEM columns (512 allocated)
-constexpr uint32_t kTmS0 = 0, kTmS1 = 64, kTmZ0 = 128, kTmZ1 = 144;
-__host__ __device__ constexpr uint32_t tm_den(int nb) { return nb ? 176u : 160u; }
-__host__ __device__ constexpr uint32_t tm_num(int nb) { return nb ? 256u : 192u; }
-constexpr uint32_t kTmT = 384;
+// TMEM columns (512 allocated): S'^T|z' (160), num|den (80), two T = Q K^T
+// buffers (128 fp32 each); P (128 x 128 bf16, two per 32-bit column) is
+// written in place over the first 64 columns of its T.
+constexpr uint32_t kTmS = 0;
+constexpr uint32_t kTmNum = 160;
+__host__ __device__ constexpr uint32_t tm_t(int b) { return b ? 384u : 256u; }
 
 // Shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t kSmPhiQ = 0;        // [blk0 16K][blk1 16K][blk2 8K]: rows = tokens
-constexpr uint32_t kSmPhiK = 40960;    // same layout
-constexpr uint32_t kSmP = 81920;       // [2][128 rows][128 B] K-major SW128
-constexpr uint32_t kSmSb = 114688;     // [160][64] bf16 MN-major SW128
-constexpr uint32_t kSmZb = 135168;     // [160][16] bf16 MN-major SW32
-constexpr uint32_t kSmOnes = 140288;   // [128][16] bf16 ones
-constexpr uint32_t kSmQ = 144384;      // 3 x [128][16] bf16 SW32
-constexpr uint32_t kSmK = 156672;      // 3 x [128][16] bf16 SW32
-constexpr uint32_t kSmV = 168960;      // 3 x [128][64] bf16 SW128
-constexpr uint32_t kSmBar = 218112;
+constexpr uint32_t kSmPhiQ = 0;        // K-major A: [blk0 16K SW128][blk1 16K SW128][blk2 8K SW64]
+constexpr uint32_t kSmPhiK = 40960;    // MN-major B: 3 x 16K SW128 (blk2: 32 of 64 features used)
+constexpr uint32_t kSmSb = 90112;      // K-major B [80 rows][160]: 2 x 10K SW128 + 5K SW64
+constexpr uint32_t kSmV = 116736;      // 3 x [128][64] bf16 SW128
+constexpr uint32_t kSmOnes = 165888;   // [128][64] bf16 ones (the extra rows/columns of [V | 1])
+constexpr uint32_t kSmQ = 182272;      // 3 x [128][16] bf16 SW32
+constexpr uint32_t kSmK = 194560;      // 3 x [128][16] bf16 SW32
+constexpr uint32_t kSmRows = 206848;   // [160] x int4 feature -> ABI row table
+constexpr uint32_t kSmBar = kSmRows + 160 * 16;
 constexpr uint32_t kSmTotal = kSmBar + 512;
 constexpr uint32_t kSmAlloc = kSmTotal + 1024;
 constexpr int kStages = 3;
@@ -71,232 +73,247 @@ constexpr int kStages = 3;
 // barrier indices
 enum {
     B_QK_FULL = 0, B_QK_EMPTY = 3, B_V_FULL = 6, B_V_EMPTY = 9,
-    B_T_FULL = 12, B_T_EMPTY, B_P_FULL, B_P_EMPTY, B_PHQ_FULL, B_PHQ_EMPTY,
-    B_PHK_FULL, B_PHK_EMPTY, B_NUM_FULL, B_NUM_EMPTY = B_NUM_FULL + 2,
-    B_S_FULL = B_NUM_EMPTY + 2, B_SB_FULL, B_FINAL, B_COUNT
+    B_T_FULL = 12,   // [2] per T buffer
+    B_PV_DONE = 14,  // [2] per T buffer: P V of that buffer completed
+    B_P_FULL = 16, B_PHQ_FULL, B_PHQ_EMPTY, B_PHK_FULL, B_PHK_EMPTY,
+    B_NUM_FULL, B_NUM_EMPTY, B_S_FULL, B_SB_FULL, B_FINAL, B_COUNT
 };
 constexpr uint32_t kSmTmemSlot = kSmBar + 8 * B_COUNT;
 constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
 static_assert(kSmAbort + 4 <= kSmTotal, "barrier area");
+static_assert(kSmSb + 25600 <= kSmV && kSmV + 3 * 16384 == kSmOnes && kSmOnes + 16384 == kSmQ &&
+              kSmQ + 3 * 4096 == kSmK && kSmK + 3 * 4096 == kSmRows, "smem map");
 
 constexpr uint32_t kIdQK = idesc_bf16(128, 128, false, false);
-constexpr uint32_t kIdPV = idesc_bf16(128, 64, false, true);
-constexpr uint32_t kIdPV16 = idesc_bf16(128, 16, false, true);
-constexpr uint32_t kIdUp = idesc_bf16(128, 64, true, true);
-constexpr uint32_t kIdUp16 = idesc_bf16(128, 16, true, true);
+constexpr uint32_t kIdPV = idesc_bf16(128, kNB, false, true);   // P (TMEM) x [V | 1]
+constexpr uint32_t kIdRO = idesc_bf16(128, kNB, false, false);  // Phi'_Q x [S' | z'] (K-major)
+constexpr uint32_t kIdUp = idesc_bf16(128, kNFeat, true, true); // [V | 1]^T x Phi'_K
 
 constexpr float kSqrt2 = 1.41421356237309504880f;
 constexpr float kRSqrt2 = 0.70710678118654752440f;
 
-// (a, b) of compact quadratic feature f: row-major over a <= b.
-__host__ __device__ constexpr int pair_a(int f) {
-    int a = 0, base = 0;
-    while (f >= base + (16 - a)) { base += 16 - a; ++a; }
-    return a;
+// Compact feature order (160 features = 80 packed bf16 pairs), chosen so that
+// every pair of quadratic features is one bf16x2 product of packed inputs:
+//   pairs  0..7   squares (2j, 2j) and (2j+1, 2j+1)
+//   pairs  8..63  for offset d = 1..15, j < (16 - d) / 2: (2j, 2j+d), (2j+1, 2j+1+d)
+//   pairs 64..67  the leftovers (4i, 15), (4i+2, 15) of the odd offsets
+//   pairs 68..75  linear xbar_{2j}, xbar_{2j+1};  pair 76: (1, 0);  77..79: 0
+// Query features are xbar_a xbar_b; key features the same except the squares,
+// which are halved, so Phi'_Q . Phi'_K = 1 + qbar.kbar + (qbar.kbar)^2 / 2.
+struct PairSpec { int kind, j, d; };  // kind 0 square, 1 off-diagonal, 2 leftover, 3 linear, 4 const, 5 zero
+__host__ __device__ constexpr PairSpec pair_spec(int r) {
+    if (r < 8) return {0, r, 0};
+    int k = 8;
+    for (int d = 1; d <= 15; ++d) {
+        const int m = (16 - d) / 2;
+        if (r < k + m) return {1, r - k, d};
+        k += m;
+    }
+    if (r < 68) return {2, r - 64, 0};
+    if (r < 76) return {3, r - 68, 0};
+    if (r == 76) return {4, 0, 0};
+    return {5, 0, 0};
 }
-__host__ __device__ constexpr int pair_b(int f) {
-    int a = pair_a(f);
-    return f - (16 * a - a * (a - 1) / 2) + a;
-}
-static_assert(pair_a(135) == 15 && pair_b(135) == 15 && pair_a(16) == 1 && pair_b(16) == 1, "");
+static_assert(pair_spec(63).kind == 1 && pair_spec(63).d == 14 && pair_spec(64).kind == 2, "layout");
 
-// Compact feature F of xbar (x / 2).  Key features halve the squares.
-template <bool kKey, int F>
-__device__ __forceinline__ float feat(const float (&x)[16]) {
-    if constexpr (F < kNQuad) {
-        constexpr int a = pair_a(F), b = pair_b(F);
-        if constexpr (kKey && a == b) return 0.5f * (x[a] * x[b]);
-        else return x[a] * x[b];
-    } else if constexpr (F == kFConst) {
-        return 1.0f;
-    } else if constexpr (F < kNReal) {
-        return x[F - kFLin];
+// (a, b) of the two quadratic features of pair r (b = -1: linear / constant / zero).
+__host__ __device__ constexpr void pair_ab(int r, int e, int &a, int &b) {
+    const PairSpec p = pair_spec(r);
+    if (p.kind == 0) { a = b = 2 * p.j + e; return; }
+    if (p.kind == 1) { a = 2 * p.j + e; b = a + p.d; return; }
+    if (p.kind == 2) { a = 4 * p.j + 2 * e; b = 15; return; }
+    a = b = -1;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(y));
+    return r;
+}
+
+// Packed features of one token: X[j] = (xbar_2j, xbar_2j+1) as bf16x2, Y[j] =
+// (xbar_2j+1, xbar_2j+2), H[j] = X[j] / 2 (keys only).
+template <bool kKey, int R>
+__device__ __forceinline__ uint32_t feat_pair(const uint32_t (&X)[8], const uint32_t (&Y)[7],
+                                              const uint32_t (&H)[8], uint32_t b15) {
+    constexpr PairSpec p = pair_spec(R);
+    if constexpr (p.kind == 0) {
+        if constexpr (kKey) return hmul2(X[p.j], H[p.j]);
+        else return hmul2(X[p.j], X[p.j]);
+    } else if constexpr (p.kind == 1) {
+        if constexpr (p.d % 2 == 0) return hmul2(X[p.j], X[p.j + p.d / 2]);
+        else return hmul2(X[p.j], Y[p.j + (p.d - 1) / 2]);
+    } else if constexpr (p.kind == 2) {
+        return hmul2(__byte_perm(X[2 * p.j], X[2 * p.j + 1], 0x5410), b15);
+    } else if constexpr (p.kind == 3) {
+        return X[p.j];
+    } else if constexpr (p.kind == 4) {
+        return 0x00003F80u;  // (1.0, 0)
     } else {
-        return 0.0f;
+        return 0u;
     }
 }
 
-// Shared-memory byte offset of 16-byte chunk J (features 8J..8J+7) of row t
-// in a feature buffer: two 128-B-swizzled 64-feature blocks + one 64-B-swizzled
-// 32-feature block.
+// Shared-memory byte offset of 16-byte chunk J (features 8J..8J+7) of token
+// row t: two 128-B-swizzled 64-feature blocks, then features 128..159 in a
+// 64-B-swizzled block (queries, K-major A) or in a 128-B-swizzled block
+// (keys, MN-major B: one 64-feature atom of which 32 are used).
+template <bool kKey>
 __device__ __forceinline__ uint32_t feat_chunk_off(int J, int t) {
     if (J < 8) return (uint32_t)(t * 128 + ((J ^ (t & 7)) << 4));
     if (J < 16) return 16384u + (uint32_t)(t * 128 + (((J - 8) ^ (t & 7)) << 4));
+    if (kKey) return 32768u + (uint32_t)(t * 128 + (((J - 16) ^ (t & 7)) << 4));
     return 32768u + (uint32_t)(t * 64 + (((J - 16) ^ ((t >> 1) & 3)) << 4));
 }
 
 template <bool kKey, int J>
-__device__ __forceinline__ void emit_chunk(const float (&x)[16], uint32_t base, int t, bool zero) {
-    uint32_t w[4];
-    w[0] = pack_bf16(feat<kKey, 8 * J + 0>(x), feat<kKey, 8 * J + 1>(x));
-    w[1] = pack_bf16(feat<kKey, 8 * J + 2>(x), feat<kKey, 8 * J + 3>(x));
-    w[2] = pack_bf16(feat<kKey, 8 * J + 4>(x), feat<kKey, 8 * J + 5>(x));
-    w[3] = pack_bf16(feat<kKey, 8 * J + 6>(x), feat<kKey, 8 * J + 7>(x));
-    if (zero) w[0] = w[1] = w[2] = w[3] = 0u;
-    st_shared_v4(base + feat_chunk_off(J, t), w[0], w[1], w[2], w[3]);
+__device__ __forceinline__ void emit_chunk(const uint32_t (&X)[8], const uint32_t (&Y)[7],
+                                           const uint32_t (&H)[8], uint32_t b15, uint32_t base, int t,
+                                           bool zero) {
+    uint32_t w0 = feat_pair<kKey, 4 * J + 0>(X, Y, H, b15);
+    uint32_t w1 = feat_pair<kKey, 4 * J + 1>(X, Y, H, b15);
+    uint32_t w2 = feat_pair<kKey, 4 * J + 2>(X, Y, H, b15);
+    uint32_t w3 = feat_pair<kKey, 4 * J + 3>(X, Y, H, b15);
+    if (zero) w0 = w1 = w2 = w3 = 0u;
+    st_shared_v4(base + feat_chunk_off<kKey>(J, t), w0, w1, w2, w3);
 }
 
 template <bool kKey, int... J>
-__device__ __forceinline__ void emit_features(const float (&x)[16], uint32_t base, int t,
+__device__ __forceinline__ void emit_features(const uint4 &lo, const uint4 &hi, uint32_t base, int t,
                                               bool zero, std::integer_sequence<int, J...>) {
-    (emit_chunk<kKey, J>(x, base, t, zero), ...);
+    // xbar = x / 2 (exact), its odd-shifted pairs, and halves for the key squares
+    const uint32_t raw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t X[8], Y[7], H[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) X[j] = hmul2(raw[j], 0x3F003F00u);
+#pragma unroll
+    for (int j = 0; j < 7; ++j) Y[j] = __byte_perm(X[j], X[j + 1], 0x5432);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) H[j] = kKey ? hmul2(X[j], 0x3F003F00u) : 0u;
+    const uint32_t b15 = __byte_perm(X[7], X[7], 0x3232);
+    (emit_chunk<kKey, J>(X, Y, H, b15, base, t, zero), ...);
 }
 
-// Read token row t (16 bf16) of a [128][16] SW32 tile as xbar = x / 2.
-__device__ __forceinline__ void load_row16(uint32_t tile, int t, float (&x)[16]) {
+// Raw token row t (16 bf16 as two 16-byte halves) of a [128][16] SW32 tile.
+__device__ __forceinline__ void load_row16_raw(uint32_t tile, int t, uint4 &lo, uint4 &hi) {
     const uint32_t sw = (uint32_t)((t >> 2) & 1);
-    const uint4 lo = ld_shared_v4(tile + t * 32 + ((0u ^ sw) << 4));
-    const uint4 hi = ld_shared_v4(tile + t * 32 + ((1u ^ sw) << 4));
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        x[2 * i] = 0.5f * bf16lo(w[i]);
-        x[2 * i + 1] = 0.5f * bf16hi(w[i]);
-    }
+    lo = ld_shared_v4(tile + t * 32 + ((0u ^ sw) << 4));
+    hi = ld_shared_v4(tile + t * 32 + ((1u ^ sw) << 4));
 }
 
 // ABI row(s) of compact feature f: r1, r2 (r2 < 0 if none); kind 0 = square,
 // 1 = off-diagonal pair, 2 = constant / linear, 3 = padding.
 struct Rows { int r1, r2, kind; };
 __device__ __forceinline__ Rows abi_rows(int f) {
-    if (f < kNQuad) {
-        int a = 0, base = 0;
-        while (f >= base + (16 - a)) { base += 16 - a; ++a; }
-        const int b = f - base + a;
+    const int r = f >> 1, e = f & 1;
+    const PairSpec p = pair_spec(r);
+    if (p.kind <= 2) {
+        int a = 0, b = 0;
+        pair_ab(r, e, a, b);
         if (a == b) return {17 + 17 * a, -1, 0};
         return {17 + 16 * a + b, 17 + 16 * b + a, 1};
     }
-    if (f == kFConst) return {0, -1, 2};
-    if (f < kNReal) return {1 + (f - kFLin), -1, 2};
+    if (p.kind == 3) return {1 + 2 * p.j + e, -1, 2};
+    if (p.kind == 4 && e == 0) return {0, -1, 2};
     return {-1, -1, 3};
 }
 
-// Compact S' row f (64 values) and z'[f] from the ABI initial state.
-__device__ __forceinline__ void load_initial(const float *s0, const float *z0, int64_t bh, int f,
-                                             float (&srow)[64], float &zf) {
-    const Rows r = abi_rows(f);
-#pragma unroll
-    for (int j = 0; j < 64; ++j) srow[j] = 0.f;
-    zf = 0.f;
-    if (!s0 || r.kind == 3) return;
-    const float4 *p1 = reinterpret_cast<const float4 *>(s0 + (bh * kD + r.r1) * kDV);
-    const float z1 = z0[bh * kD + r.r1];
-    if (r.kind == 2) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float4 a = p1[j];
-            srow[4 * j] = a.x; srow[4 * j + 1] = a.y; srow[4 * j + 2] = a.z; srow[4 * j + 3] = a.w;
-        }
-        zf = z1;
-    } else if (r.kind == 0) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float4 a = p1[j];
-            srow[4 * j] = a.x * kRSqrt2; srow[4 * j + 1] = a.y * kRSqrt2;
-            srow[4 * j + 2] = a.z * kRSqrt2; srow[4 * j + 3] = a.w * kRSqrt2;
-        }
-        zf = z1 * kRSqrt2;
-    } else {
-        const float4 *p2 = reinterpret_cast<const float4 *>(s0 + (bh * kD + r.r2) * kDV);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float4 a = p1[j], b = p2[j];
-            srow[4 * j] = (a.x + b.x) * kRSqrt2; srow[4 * j + 1] = (a.y + b.y) * kRSqrt2;
-            srow[4 * j + 2] = (a.z + b.z) * kRSqrt2; srow[4 * j + 3] = (a.w + b.w) * kRSqrt2;
-        }
-        zf = (z1 + z0[bh * kD + r.r2]) * kRSqrt2;
-    }
+// Compact entry of the initial state for feature row f (r = its ABI rows):
+// squares carry 1/sqrt2, pairs the symmetric sum over (a,b) and (b,a).
+__device__ __forceinline__ float compact_initial(const float *col, int stride, const Rows &r) {
+    if (!col || r.kind == 3) return 0.f;
+    const float a = col[(int64_t)r.r1 * stride];
+    if (r.kind == 2) return a;
+    if (r.kind == 0) return a * kRSqrt2;
+    return (a + col[(int64_t)r.r2 * stride]) * kRSqrt2;
 }
 
-// Write compact row f of the final state back to the ABI layout.
-__device__ __forceinline__ void store_final(const float *s0, const float *z0, float *s_out,
-                                            float *z_out, int64_t bh, int f,
-                                            const float (&srow)[64], float zf) {
-    const Rows r = abi_rows(f);
-    if (r.kind == 3) return;
-    if (r.kind == 1) {
-        // S'/sqrt2 is the symmetric part; the antisymmetric part of s0 passes through.
-        float4 *o1 = s_out ? reinterpret_cast<float4 *>(s_out + (bh * kD + r.r1) * kDV) : nullptr;
-        float4 *o2 = s_out ? reinterpret_cast<float4 *>(s_out + (bh * kD + r.r2) * kDV) : nullptr;
-        const float4 *a1 = s0 ? reinterpret_cast<const float4 *>(s0 + (bh * kD + r.r1) * kDV) : nullptr;
-        const float4 *a2 = s0 ? reinterpret_cast<const float4 *>(s0 + (bh * kD + r.r2) * kDV) : nullptr;
-        if (o1) {
+// Final ABI entries from compact value x: squares sqrt2 x; pairs x/sqrt2 plus
+// and minus half the antisymmetric part of the initial state.
+__device__ __forceinline__ void store_compact(const float *col0, float *out, int stride,
+                                              const Rows &r, float x) {
+    if (!out || r.kind == 3) return;
+    if (r.kind == 2) { out[(int64_t)r.r1 * stride] = x; return; }
+    if (r.kind == 0) { out[(int64_t)r.r1 * stride] = x * kSqrt2; return; }
+    const float sym = x * kRSqrt2;
+    const float anti = col0 ? 0.5f * (col0[(int64_t)r.r1 * stride] - col0[(int64_t)r.r2 * stride]) : 0.f;
+    out[(int64_t)r.r1 * stride] = sym + anti;
+    out[(int64_t)r.r2 * stride] = sym - anti;
+}
+
+// Byte offset of 16-byte chunk j (features 8j..8j+7) of row d in the K-major
+// [80][160] state operand.
+__device__ __forceinline__ uint32_t sb_chunk_off(int d, int j) {
+    if (j < 8) return (uint32_t)(d * 128 + ((j ^ (d & 7)) << 4));
+    if (j < 16) return 10240u + (uint32_t)(d * 128 + (((j - 8) ^ (d & 7)) << 4));
+    return 20480u + (uint32_t)(d * 64 + (((j - 16) ^ ((d >> 1) & 3)) << 4));
+}
+
+// Write 32 consecutive features (group g) of state row d as bf16.
+__device__ __forceinline__ void write_sb_group(uint32_t sbase, int d, int g, const uint32_t (&r)[32]) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float4 sym = make_float4(srow[4 * j] * kRSqrt2, srow[4 * j + 1] * kRSqrt2,
-                                         srow[4 * j + 2] * kRSqrt2, srow[4 * j + 3] * kRSqrt2);
-                float4 anti = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (a1) {
-                    const float4 x = a1[j], y = a2[j];
-                    anti = make_float4(0.5f * (x.x - y.x), 0.5f * (x.y - y.y), 0.5f * (x.z - y.z),
-                                       0.5f * (x.w - y.w));
-                }
-                o1[j] = make_float4(sym.x + anti.x, sym.y + anti.y, sym.z + anti.z, sym.w + anti.w);
-                o2[j] = make_float4(sym.x - anti.x, sym.y - anti.y, sym.z - anti.z, sym.w - anti.w);
+    for (int q = 0; q < 4; ++q)
+        st_shared_v4(sbase + sb_chunk_off(d, 4 * g + q),
+                     pack_bf16(__uint_as_float(r[8 * q + 0]), __uint_as_float(r[8 * q + 1])),
+                     pack_bf16(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                     pack_bf16(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                     pack_bf16(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+}
+
+// Final ABI state from TMEM rows, for one warp's lanes and feature groups
+// [g0, g0 + ng): value rows d < 64, and the z' row (lane 64, by lane 0 of the
+// warp that owns lanes 64..95).  Runs once per CTA, so it is kept out of line.
+__device__ __noinline__ void store_final_groups(uint32_t taddr, int g0, int ng, int d, bool zrow, int lane,
+                                                const int4 *rows_tab, const float *s0h, float *s_outh,
+                                                const float *z0h, float *z_outh) {
+    for (int g = g0; g < g0 + ng; ++g) {
+        uint32_t r[32];
+        tmem_load32_sync(taddr + 32 * g, r);
+        if (!zrow || lane == 0) {
+            for (int j = 0; j < 32; ++j) {
+                const int4 e = rows_tab[32 * g + j];
+                if (zrow) store_compact(z0h, z_outh, 1, Rows{e.x, e.y, e.z}, __uint_as_float(r[j]));
+                else store_compact(s0h ? s0h + d : nullptr, s_outh ? s_outh + d : nullptr, kDV,
+                                   Rows{e.x, e.y, e.z}, __uint_as_float(r[j]));
             }
         }
-        if (z_out) {
-            const float sym = zf * kRSqrt2;
-            const float anti = z0 ? 0.5f * (z0[bh * kD + r.r1] - z0[bh * kD + r.r2]) : 0.f;
-            z_out[bh * kD + r.r1] = sym + anti;
-            z_out[bh * kD + r.r2] = sym - anti;
-        }
-        return;
-    }
-    const float sc = r.kind == 0 ? kSqrt2 : 1.0f;
-    if (s_out) {
-        float4 *o = reinterpret_cast<float4 *>(s_out + (bh * kD + r.r1) * kDV);
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            o[j] = make_float4(srow[4 * j] * sc, srow[4 * j + 1] * sc, srow[4 * j + 2] * sc,
-                               srow[4 * j + 3] * sc);
-    }
-    if (z_out) z_out[bh * kD + r.r1] = zf * sc;
-}
-
-// bf16 copy of S' row f (64 values) into the MN-major SW128 operand, and z'[f]
-// into column 0 of the [160][16] SW32 operand.
-__device__ __forceinline__ void write_state_operand(uint32_t sb, uint32_t zb, int f,
-                                                    const float (&srow)[64], float zf) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        st_shared_v4(sb + f * 128 + ((j ^ (f & 7)) << 4),
-                     pack_bf16(srow[8 * j + 0], srow[8 * j + 1]),
-                     pack_bf16(srow[8 * j + 2], srow[8 * j + 3]),
-                     pack_bf16(srow[8 * j + 4], srow[8 * j + 5]),
-                     pack_bf16(srow[8 * j + 6], srow[8 * j + 7]));
-    }
-    st_shared_v4(zb + f * 32 + (((f >> 2) & 1) << 4), pack_bf16(zf, 0.f), 0u, 0u, 0u);
-}
-
-__device__ __forceinline__ void tmem_load_row64(uint32_t taddr, float (&srow)[64]) {
-    uint32_t r0[32], r1[32];
-    tmem_ld32(taddr, r0);
-    tmem_ld32(taddr + 32, r1);
-    tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        srow[j] = __uint_as_float(r0[j]);
-        srow[32 + j] = __uint_as_float(r1[j]);
+        __syncwarp();
     }
 }
 
-__device__ __forceinline__ void tmem_store_row64(uint32_t taddr, const float (&srow)[64]) {
-    uint32_t r[32];
+// bf16 operand rows of the state after a chunk, for one warp's TMEM lanes and
+// feature groups [kG0, kG0 + kNG) (32 features each): value rows d < 64 and
+// the z' row 64 (lane 0 of the warp owning lanes 64..95).
+template <int kG0, int kNG>
+__device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, int d, bool zrow, int lane) {
+    uint32_t r[32 * kNG];
+    if constexpr (kNG == 2) {
+        uint32_t (&r64)[64] = reinterpret_cast<uint32_t (&)[64]>(r);
+        tmem_load64_sync(taddr + 32 * kG0, r64);
+    } else {
+        uint32_t (&r32)[32] = reinterpret_cast<uint32_t (&)[32]>(r);
+        tmem_load32_sync(taddr + 32 * kG0, r32);
+    }
+    if (zrow && lane != 0) return;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(srow[j]);
-    tmem_st32(taddr, r);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(srow[32 + j]);
-    tmem_st32(taddr + 32, r);
+    for (int g = 0; g < kNG; ++g)
+        write_sb_group(sbase, zrow ? 64 : d, kG0 + g, *reinterpret_cast<const uint32_t (*)[32]>(r + 32 * g));
 }
 
-__device__ __forceinline__ void tmem_store_z16(uint32_t taddr, float zf) {
-    uint32_t r[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(zf);
-    tmem_st16(taddr, r);
-}
+// Optional per-role timeline of CTA 0 (compile with -DLA_TRACE): SM clock
+// offsets from kernel entry for events of each role and chunk.
+constexpr int kTraceChunks = 512;
+#ifdef LA_TRACE
+__device__ uint32_t g_trace[5][kTraceChunks][8];
+#define LA_TR(role, c, ev)                                                         \
+    do {                                                                           \
+        if (blockIdx.x == 0 && (c) < kTraceChunks)                                 \
+            g_trace[role][c][ev] = (uint32_t)(clock64() - t_start);                \
+    } while (0)
+#else
+#define LA_TR(role, c, ev) do { } while (0)
+#endif
+enum { TR_TMA = 0, TR_MMA, TR_GEN, TR_EPI, TR_CONV };
 
 // Drain wait used when unwinding: bounded, ignores the abort flag.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -317,12 +334,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const uint32_t sb = smem_u32(smem);
     auto bar = [&](int i) { return sb + kSmBar + 8u * (uint32_t)i; };
     volatile int *abort = reinterpret_cast<volatile int *>(smem + kSmAbort);
+    const int4 *rows_tab = reinterpret_cast<const int4 *>(smem + kSmRows);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t bh = blockIdx.x;
+#ifdef LA_TRACE
+    const long long t_start = clock64();
+#endif
     const int n = (N + kC - 1) / kC;
+    // per-head columns of the ABI state: entry (row r, value d) at [r * 64 + d]
+    const float *s0h = s0 ? s0 + bh * (int64_t)kD * kDV : nullptr;
+    const float *z0h = z0 ? z0 + bh * (int64_t)kD : nullptr;
+    float *s_outh = s_out ? s_out + bh * (int64_t)kD * kDV : nullptr;
+    float *z_outh = z_out ? z_out + bh * (int64_t)kD : nullptr;
 
-    // ---- set-up: barriers, TMEM, constant operands
+    // ---- set-up: barriers, TMEM, constant operands, feature -> row table
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_QK_FULL + s), 1);
@@ -330,20 +356,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
-        mbar_init(bar(B_T_FULL), 1);
-        mbar_init(bar(B_T_EMPTY), 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(B_T_FULL + i), 1);
+            mbar_init(bar(B_PV_DONE + i), 1);
+        }
         mbar_init(bar(B_P_FULL), 4);
-        mbar_init(bar(B_P_EMPTY), 1);
         mbar_init(bar(B_PHQ_FULL), 4);
         mbar_init(bar(B_PHQ_EMPTY), 1);
         mbar_init(bar(B_PHK_FULL), 4);
         mbar_init(bar(B_PHK_EMPTY), 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_NUM_FULL + i), 1);
-            mbar_init(bar(B_NUM_EMPTY + i), 4);
-        }
+        mbar_init(bar(B_NUM_FULL), 1);
+        mbar_init(bar(B_NUM_EMPTY), 4);
         mbar_init(bar(B_S_FULL), 1);
-        mbar_init(bar(B_SB_FULL), 4);
+        mbar_init(bar(B_SB_FULL), 8);
         mbar_init(bar(B_FINAL), 1);
         *abort = 0;
         mbar_init_fence();
@@ -352,15 +377,50 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         tmem_alloc(sb + kSmTmemSlot, 512);
         tmem_relinquish();
     }
-    // ones operand, and zero the z' operand (only its column 0 is rewritten later)
-    for (int i = tid; i < 4096 / 16; i += kThreads)
+    for (int i = tid; i < 16384 / 16; i += kThreads)
         st_shared_v4(sb + kSmOnes + 16 * i, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    for (int i = tid; i < 5120 / 16; i += kThreads) st_shared_v4(sb + kSmZb + 16 * i, 0u, 0u, 0u, 0u);
+    // rows 65..79 of the state operand stay zero (only the z' row 64 is used)
+    for (int i = tid; i < 15 * 20; i += kThreads) {
+        const int d = 65 + i / 20, j = i % 20;
+        st_shared_v4(sb + kSmSb + sb_chunk_off(d, j), 0u, 0u, 0u, 0u);
+    }
+    if (tid < kNFeat) {
+        const Rows r = abi_rows(tid);
+        reinterpret_cast<int4 *>(smem + kSmRows)[tid] = make_int4(r.r1, r.r2, r.kind, 0);
+    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kSmTmemSlot);
+
+    // initial state, before any role starts: S'^T rows (values d = 0..63, lanes of
+    // warps 12, 13) and z' (lanes 64.., warp 14) in TMEM, and their bf16 operand rows
+    if (warp >= 12 && warp < 15) {
+        const int w = warp - 12;
+        const int d = 32 * w + lane;
+        const bool zrow = (w == 2);
+        const uint32_t lanebase = (uint32_t)(32 * w) << 16;
+#pragma unroll 1
+        for (int g = 0; g < kNFeat / 32; ++g) {
+            uint32_t r[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int4 e = rows_tab[32 * g + j];
+                const Rows rw{e.x, e.y, e.z};
+                const float x = zrow ? compact_initial(z0h, 1, rw)
+                                     : compact_initial(s0h ? s0h + d : nullptr, kDV, rw);
+                r[j] = __float_as_uint(x);
+            }
+            __syncwarp();
+            tmem_store32_sync(tmem + lanebase + kTmS + 32 * g, r);
+            if (!zrow || lane == 0) write_sb_group(sb + kSmSb, zrow ? 64 : d, g, r);
+        }
+        fence_async_smem();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
 
     if (warp == 0) {
         // ================= TMA producer =================
@@ -373,11 +433,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const int st = c % kStages;
                 const uint32_t ph = ((uint32_t)(c / kStages) & 1u) ^ 1u;
                 if (!mbar_wait(bar(B_QK_EMPTY + st), ph, abort, status)) break;
+                LA_TR(TR_TMA, c, 0);
                 mbar_expect_tx(bar(B_QK_FULL + st), 2 * kC * 16 * 2);
                 tma_load_3d(sb + kSmQ + st * 4096, &tq, bar(B_QK_FULL + st), 0, c * kC, (int)bh);
                 tma_load_3d(sb + kSmK + st * 4096, &tk, bar(B_QK_FULL + st), 0, c * kC, (int)bh);
                 issued_qk = c + 1;
                 if (!mbar_wait(bar(B_V_EMPTY + st), ph, abort, status)) break;
+                LA_TR(TR_TMA, c, 1);
                 mbar_expect_tx(bar(B_V_FULL + st), kC * 64 * 2);
                 tma_load_3d(sb + kSmV + st * 16384, &tv, bar(B_V_FULL + st), 0, c * kC, (int)bh);
                 issued_v = c + 1;
@@ -394,86 +456,87 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            auto qdesc = [&](int st) { return smem_desc(sb + kSmQ + st * 4096, 16, 256, kSw32); };
-            auto kdesc = [&](int st) { return smem_desc(sb + kSmK + st * 4096, 16, 256, kSw32); };
-            auto vdesc = [&](int st, int s) {
-                return smem_desc(sb + kSmV + st * 16384 + s * 2048, 16384, 1024, kSw128);
+            // descriptor bases; per-step offsets are added in 16-byte units
+            const uint64_t dQ = smem_desc(sb + kSmQ, 16, 256, kSw32);
+            const uint64_t dK = smem_desc(sb + kSmK, 16, 256, kSw32);
+            const uint64_t dPhiQ = smem_desc(sb + kSmPhiQ, 16, 1024, kSw128);
+            const uint64_t dPhiQ2 = smem_desc(sb + kSmPhiQ + 32768, 16, 512, kSw64);
+            const uint64_t dSb = smem_desc(sb + kSmSb, 16, 1024, kSw128);
+            const uint64_t dSb2 = smem_desc(sb + kSmSb + 20480, 16, 512, kSw64);
+            const uint64_t dPhiK = smem_desc(sb + kSmPhiK, 16384, 1024, kSw128);
+            // [V | 1]: V stage st plus the ones atom at a fixed distance past it;
+            // the B operand of P V and (as MN-major A) of the state update
+            const uint64_t dV0 = smem_desc(sb + kSmV, kSmOnes - kSmV, 1024, kSw128);
+            auto dVst = [&](int st) {
+                return dV0 + (uint64_t)(st * (16384 >> 4)) - ((uint64_t)(st * (16384 >> 4)) << 16);
             };
-            auto onesdesc = [&](int s) { return smem_desc(sb + kSmOnes + s * 512, 4096, 256, kSw32); };
-            auto pdesc = [&](int s) {
-                return smem_desc(sb + kSmP + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSw128);
+            auto issue_qk = [&](int c) {  // T[c & 1] = Q_c K_c^T
+                const int st = c % kStages;
+                mma_bf16(tmem + tm_t(c & 1), dQ + st * (4096 >> 4), dK + st * (4096 >> 4), kIdQK, 0);
+                mma_commit(bar(B_T_FULL + (c & 1)));
+                mma_commit(bar(B_QK_EMPTY + st));
             };
-            auto phiqdesc = [&](int s) {
-                return s < 8 ? smem_desc(sb + kSmPhiQ + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSw128)
-                             : smem_desc(sb + kSmPhiQ + 32768 + (s - 8) * 32, 16, 512, kSw64);
-            };
-            auto sbdesc = [&](int s) { return smem_desc(sb + kSmSb + s * 2048, 16384, 1024, kSw128); };
-            auto zbdesc = [&](int s) { return smem_desc(sb + kSmZb + s * 512, 4096, 256, kSw32); };
-            auto phik0desc = [&](int s) { return smem_desc(sb + kSmPhiK + s * 2048, 16384, 1024, kSw128); };
-            auto phik1desc = [&](int s) { return smem_desc(sb + kSmPhiK + 32768 + s * 1024, 8192, 512, kSw64); };
-
             bool ok = mbar_wait(bar(B_QK_FULL + 0), 0, abort, status);
             if (ok) {
                 tc_fence_after();
-                mma_bf16(tmem + kTmT, qdesc(0), kdesc(0), kIdQK, 0);
-                mma_commit(bar(B_T_FULL));
-                mma_commit(bar(B_QK_EMPTY + 0));
+                issue_qk(0);
             }
             for (int c = 0; ok && c < n; ++c) {
-                const int vs = c % kStages, nb = c & 1;
+                const int vs = c % kStages, b = c & 1;
+                const uint64_t dV = dVst(vs);
                 const uint32_t pc = (uint32_t)c & 1u;
+                // P(c) is in T[b]; V(c) is in; num was drained for chunk c - 1
                 ok = mbar_wait(bar(B_P_FULL), pc, abort, status) &&
                      mbar_wait(bar(B_V_FULL + vs), (uint32_t)(c / kStages) & 1u, abort, status) &&
-                     mbar_wait(bar(B_NUM_EMPTY + nb), ((uint32_t)(c >> 1) & 1u) ^ 1u, abort, status);
+                     mbar_wait(bar(B_NUM_EMPTY), pc ^ 1u, abort, status);
                 if (!ok) break;
+                LA_TR(TR_MMA, c, 0);
                 tc_fence_after();
-                // intra-chunk: num = P V, den = P 1
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    mma_bf16(tmem + tm_num(nb), pdesc(s), vdesc(vs, s), kIdPV, s > 0);
-                    mma_bf16(tmem + tm_den(nb), pdesc(s), onesdesc(s), kIdPV16, s > 0);
-                }
-                mma_commit(bar(B_P_EMPTY));
-                // next chunk's Q K^T as soon as its tiles are in
+                // next chunk's Q K^T into the other T buffer, once P V of chunk c - 1 left it
                 if (c + 1 < n) {
-                    const int st = (c + 1) % kStages;
-                    ok = mbar_wait(bar(B_QK_FULL + st), (uint32_t)((c + 1) / kStages) & 1u, abort, status) &&
-                         mbar_wait(bar(B_T_EMPTY), pc, abort, status);
+                    ok = mbar_wait(bar(B_QK_FULL + (c + 1) % kStages), (uint32_t)((c + 1) / kStages) & 1u,
+                                   abort, status) &&
+                         (c == 0 || mbar_wait(bar(B_PV_DONE + (b ^ 1)), (uint32_t)((c - 1) >> 1) & 1u,
+                                              abort, status));
                     if (!ok) break;
                     tc_fence_after();
-                    mma_bf16(tmem + kTmT, qdesc(st), kdesc(st), kIdQK, 0);
-                    mma_commit(bar(B_T_FULL));
-                    mma_commit(bar(B_QK_EMPTY + st));
+                    issue_qk(c + 1);
                 }
-                // inter-chunk read-out: num += Phi'_Q S', den += Phi'_Q z'
+                LA_TR(TR_MMA, c, 1);
+                // intra-chunk: [num | den] = P [V | 1], P from TMEM
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_bf16_ts(tmem + kTmNum, tmem + tm_t(b) + 8 * s, dV + s * (2048 >> 4), kIdPV, s > 0);
+                mma_commit(bar(B_PV_DONE + b));
+                // inter-chunk read-out: [num | den] += Phi'_Q [S' | z'] (both K-major)
                 ok = mbar_wait(bar(B_SB_FULL), pc, abort, status) &&
                      mbar_wait(bar(B_PHQ_FULL), pc, abort, status);
                 if (!ok) break;
+                LA_TR(TR_MMA, c, 2);
                 tc_fence_after();
 #pragma unroll
-                for (int s = 0; s < 10; ++s) {
-                    mma_bf16(tmem + tm_num(nb), phiqdesc(s), sbdesc(s), kIdPV, 1);
-                    mma_bf16(tmem + tm_den(nb), phiqdesc(s), zbdesc(s), kIdPV16, 1);
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t o = (uint32_t)((s >> 2) * 16384 + (s & 3) * 32) >> 4;
+                    const uint32_t ob = (uint32_t)((s >> 2) * 10240 + (s & 3) * 32) >> 4;
+                    mma_bf16(tmem + kTmNum, dPhiQ + o, dSb + ob, kIdRO, 1);
                 }
-                mma_commit(bar(B_NUM_FULL + nb));
+#pragma unroll
+                for (int s = 8; s < 10; ++s)
+                    mma_bf16(tmem + kTmNum, dPhiQ2 + ((s - 8) * 32 >> 4), dSb2 + ((s - 8) * 32 >> 4), kIdRO, 1);
+                mma_commit(bar(B_NUM_FULL));
                 mma_commit(bar(B_PHQ_EMPTY));
-                // state update: S' += Phi'_K^T V, z' += Phi'_K^T 1
+                // state update: [S'^T ; z'] += [V | 1]^T Phi'_K, 16 tokens per MMA
                 ok = mbar_wait(bar(B_PHK_FULL), pc, abort, status);
                 if (!ok) break;
+                LA_TR(TR_MMA, c, 3);
                 tc_fence_after();
 #pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    mma_bf16(tmem + kTmS0, phik0desc(s), vdesc(vs, s), kIdUp, 1);
-                    mma_bf16(tmem + kTmZ0, phik0desc(s), onesdesc(s), kIdUp16, 1);
-                }
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    mma_bf16(tmem + kTmS1, phik1desc(s), vdesc(vs, s), kIdUp, 1);
-                    mma_bf16(tmem + kTmZ1, phik1desc(s), onesdesc(s), kIdUp16, 1);
-                }
+                for (int s = 0; s < 8; ++s)
+                    mma_bf16(tmem + kTmS, dV + s * (2048 >> 4), dPhiK + s * (2048 >> 4), kIdUp, 1);
                 mma_commit(bar(B_S_FULL));
                 mma_commit(bar(B_PHK_EMPTY));
                 mma_commit(bar(B_V_EMPTY + vs));
+                LA_TR(TR_MMA, c, 4);
             }
             // every issued MMA must finish before TMEM is released
             mma_commit(bar(B_FINAL));
@@ -486,152 +549,151 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const int st = c % kStages;
             const uint32_t pc = (uint32_t)c & 1u;
             if (!mbar_wait(bar(B_QK_FULL + st), (uint32_t)(c / kStages) & 1u, abort, status)) break;
-            float xq[16], xk[16];
-            load_row16(sb + kSmQ + st * 4096, t, xq);
-            load_row16(sb + kSmK + st * 4096, t, xk);
+            if (tid == 128) LA_TR(TR_GEN, c, 0);
+            uint4 qlo, qhi, klo, khi;
+            load_row16_raw(sb + kSmQ + st * 4096, t, qlo, qhi);
+            load_row16_raw(sb + kSmK + st * 4096, t, klo, khi);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_QK_EMPTY + st));
             if (!mbar_wait(bar(B_PHQ_EMPTY), pc ^ 1u, abort, status)) break;
-            emit_features<false>(xq, sb + kSmPhiQ, t, false, std::make_integer_sequence<int, 20>{});
+            emit_features<false>(qlo, qhi, sb + kSmPhiQ, t, false, std::make_integer_sequence<int, 20>{});
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PHQ_FULL));
+            if (tid == 128) LA_TR(TR_GEN, c, 1);
             const bool pad = c * kC + t >= N;  // past the end: no contribution to S', z'
             if (!mbar_wait(bar(B_PHK_EMPTY), pc ^ 1u, abort, status)) break;
-            emit_features<true>(xk, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
+            if (tid == 128) LA_TR(TR_GEN, c, 2);
+            emit_features<true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PHK_FULL));
+            if (tid == 128) LA_TR(TR_GEN, c, 3);
         }
     } else if (warp >= 8 && warp < 12) {
-        // ================= P epilogue and output epilogue =================
+        // ================= P epilogue: P = 1 + T/4 + T^2/32, causal, in place =================
         const int w = warp - 8;
         const int i = tid - 256;  // query row within the chunk (= TMEM lane)
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
+        const bool zrow = (w == 2);  // warp 10: lane 64 holds z'
         auto do_p = [&](int c) -> bool {
-            const uint32_t pc = (uint32_t)c & 1u;
-            if (!mbar_wait(bar(B_T_FULL), pc, abort, status)) return false;
-            if (!mbar_wait(bar(B_P_EMPTY), pc ^ 1u, abort, status)) return false;
+            const int b = c & 1;
+            if (!mbar_wait(bar(B_T_FULL + b), (uint32_t)(c >> 1) & 1u, abort, status)) return false;
+            if (tid == 256 + 96) LA_TR(TR_EPI, c, 0);
+            __syncwarp();  // tcgen05.ld/st below are warp-collective (.sync.aligned)
             tc_fence_after();
+            const uint32_t tb = tmem + lanebase + tm_t(b);
+            // keys 64 pp .. 64 pp + 63 -> packed columns 32 pp .. 32 pp + 31, written only
+            // after the T columns they overwrite have been read; rows of warp w only see
+            // keys < 32 (w + 1)
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                uint32_t pw[16];
-                if (p <= w) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lanebase + kTmT + 32 * p, r);
-                    tmem_wait_ld();
+            for (int pp = 0; pp < 2; ++pp) {
+                uint32_t pw[32];
+                if (2 * pp <= w) {
+                    uint32_t r[64];
+                    tmem_load64_sync(tb + 64 * pp, r);
+                    const uint64_t c32 = f2pack(0.03125f, 0.03125f), c4 = f2pack(0.25f, 0.25f),
+                                   c1 = f2pack(1.0f, 1.0f);
+                    const bool diag = 64 * pp + 63 >= 32 * w;  // this block reaches the diagonal
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float t0 = __uint_as_float(r[2 * j]), t1 = __uint_as_float(r[2 * j + 1]);
-                        float p0 = fmaf(t0, fmaf(t0, 0.03125f, 0.25f), 1.0f);
-                        float p1 = fmaf(t1, fmaf(t1, 0.03125f, 0.25f), 1.0f);
-                        if (p == w) {
-                            if (32 * p + 2 * j > i) p0 = 0.f;
-                            if (32 * p + 2 * j + 1 > i) p1 = 0.f;
+                    for (int j = 0; j < 32; ++j) {
+                        const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
+                        const uint64_t p2 = ffma2(t2, ffma2(t2, c32, c4), c1);
+                        float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
+                        if (diag) {
+                            const int key = 64 * pp + 2 * j;
+                            if (key > i) p0 = 0.f;
+                            if (key + 1 > i) p1 = 0.f;
                         }
                         pw[j] = pack_bf16(p0, p1);
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) pw[j] = 0u;
+                    for (int j = 0; j < 32; ++j) pw[j] = 0u;
                 }
-                const uint32_t blk = sb + kSmP + (uint32_t)(p >> 1) * 16384 + i * 128;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int J = (p & 1) * 4 + q;
-                    st_shared_v4(blk + ((J ^ (i & 7)) << 4), pw[4 * q], pw[4 * q + 1], pw[4 * q + 2],
-                                 pw[4 * q + 3]);
-                }
+                tmem_store32_sync(tb + 32 * pp, pw);
             }
-            fence_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(bar(B_T_EMPTY));
-                mbar_arrive(bar(B_P_FULL));
-            }
+            if (lane == 0) mbar_arrive(bar(B_P_FULL));
+            if (tid == 256 + 96) LA_TR(TR_EPI, c, 1);
             return true;
         };
-        auto do_y = [&](int c) -> bool {
-            const int nb = c & 1;
-            if (!mbar_wait(bar(B_NUM_FULL + nb), (uint32_t)(c >> 1) & 1u, abort, status)) return false;
-            tc_fence_after();
-            uint32_t r0[32], r1[32], dr;
-            tmem_ld32(tmem + lanebase + tm_num(nb), r0);
-            tmem_ld32(tmem + lanebase + tm_num(nb) + 32, r1);
-            tmem_ld1(tmem + lanebase + tm_den(nb), dr);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_NUM_EMPTY + nb));
-            const int row = c * kC + i;
-            if (row < N) {
-                const float inv = 1.0f / (__uint_as_float(dr) + eps);
-                uint4 *dst = reinterpret_cast<uint4 *>(y + ((int64_t)bh * N + row) * kDV);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    dst[j] = make_uint4(
-                        pack_bf16(__uint_as_float(r0[8 * j + 0]) * inv, __uint_as_float(r0[8 * j + 1]) * inv),
-                        pack_bf16(__uint_as_float(r0[8 * j + 2]) * inv, __uint_as_float(r0[8 * j + 3]) * inv),
-                        pack_bf16(__uint_as_float(r0[8 * j + 4]) * inv, __uint_as_float(r0[8 * j + 5]) * inv),
-                        pack_bf16(__uint_as_float(r0[8 * j + 6]) * inv, __uint_as_float(r0[8 * j + 7]) * inv));
-                    dst[4 + j] = make_uint4(
-                        pack_bf16(__uint_as_float(r1[8 * j + 0]) * inv, __uint_as_float(r1[8 * j + 1]) * inv),
-                        pack_bf16(__uint_as_float(r1[8 * j + 2]) * inv, __uint_as_float(r1[8 * j + 3]) * inv),
-                        pack_bf16(__uint_as_float(r1[8 * j + 4]) * inv, __uint_as_float(r1[8 * j + 5]) * inv),
-                        pack_bf16(__uint_as_float(r1[8 * j + 6]) * inv, __uint_as_float(r1[8 * j + 7]) * inv));
-                }
-            }
-            return true;
-        };
+        if (lane == 0) mbar_arrive(bar(B_SB_FULL));  // phase 0: initial operand written in set-up
         if (do_p(0)) {
             for (int c = 0; c < n; ++c) {
                 if (c + 1 < n && !do_p(c + 1)) break;
-                if (!do_y(c)) break;
+                // second part of the state conversion: feature groups 3, 4
+                if (!mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status)) break;
+                __syncwarp();
+                tc_fence_after();
+                const bool last = (c == n - 1);
+                if (w < 3) {
+                    if (!last) convert_groups<3, 2>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane);
+                    else store_final_groups(tmem + lanebase + kTmS, 3, 2, i, zrow, lane, rows_tab, s0h,
+                                            s_outh, z0h, z_outh);
+                }
+                __syncwarp();
+                if (!last) {
+                    fence_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_SB_FULL));
+                }
             }
         }
     } else if (warp >= 12) {
-        // ================= state conversion =================
+        // ========== output epilogue y = num / den, then state conversion ==========
         const int w = warp - 12;
-        const int f = 32 * w + lane;          // compact feature of TMEM tile 0 (lane f)
-        const int f1 = 128 + lane;            // compact feature of tile 1 (warp 12 only)
+        const int i = 32 * w + lane;          // query row (num lane) / value row d of S'^T
+        const bool zrow = (w == 2);           // warp 14: lane 64 holds z'
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
-        {
-            float srow[64], zf;
-            load_initial(s0, z0, bh, f, srow, zf);
-            tmem_store_row64(tmem + lanebase + kTmS0, srow);
-            tmem_store_z16(tmem + lanebase + kTmZ0, zf);
-            write_state_operand(sb + kSmSb, sb + kSmZb, f, srow, zf);
-            if (w == 0) {
-                load_initial(s0, z0, bh, f1, srow, zf);
-                tmem_store_row64(tmem + kTmS1, srow);
-                tmem_store_z16(tmem + kTmZ1, zf);
-                write_state_operand(sb + kSmSb, sb + kSmZb, f1, srow, zf);
-            }
-            tmem_wait_st();
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_SB_FULL));
-        }
+        if (lane == 0) mbar_arrive(bar(B_SB_FULL));  // phase 0: initial operand written in set-up
         for (int c = 0; c < n; ++c) {
-            if (!mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status)) break;
+            // ---- y(c)
+            if (!mbar_wait(bar(B_NUM_FULL), (uint32_t)c & 1u, abort, status)) break;
+            if (tid == 384) LA_TR(TR_EPI, c, 2);
+            __syncwarp();
             tc_fence_after();
-            float srow[64];
-            uint32_t zr;
-            const bool last = (c == n - 1);
-            tmem_ld1(tmem + lanebase + kTmZ0, zr);
-            tmem_load_row64(tmem + lanebase + kTmS0, srow);
-            if (!last) {
-                write_state_operand(sb + kSmSb, sb + kSmZb, f, srow, __uint_as_float(zr));
-            } else {
-                store_final(s0, z0, s_out, z_out, bh, f, srow, __uint_as_float(zr));
+            {
+                uint32_t r[64], dr;
+                tmem_load64_1_sync(tmem + lanebase + kTmNum, 64, r, dr);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_NUM_EMPTY));
+                const int row = c * kC + i;
+                if (row < N) {
+                    const float inv = 1.0f / (__uint_as_float(dr) + eps);
+                    const uint64_t inv2 = f2pack(inv, inv);
+                    uint4 *dst = reinterpret_cast<uint4 *>(y + ((int64_t)bh * N + row) * kDV);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t o[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h)
+                            o[h] = pack_bf16x2(fmul2((uint64_t)r[8 * j + 2 * h] | ((uint64_t)r[8 * j + 2 * h + 1] << 32),
+                                                     inv2));
+                        dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
             }
-            if (w == 0) {
-                tmem_ld1(tmem + kTmZ1, zr);
-                tmem_load_row64(tmem + kTmS1, srow);
-                if (!last) write_state_operand(sb + kSmSb, sb + kSmZb, f1, srow, __uint_as_float(zr));
-                else store_final(s0, z0, s_out, z_out, bh, f1, srow, __uint_as_float(zr));
+            if (tid == 384) LA_TR(TR_EPI, c, 3);
+            // ---- state after chunk c: bf16 operand for the next read-out, or the final state
+            if (!mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status)) break;
+            if (tid == 384) LA_TR(TR_CONV, c, 0);
+            __syncwarp();
+            tc_fence_after();
+            const bool last = (c == n - 1);
+            if (w < 3) {
+                if (!last) {
+                    convert_groups<0, 2>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane);
+                    __syncwarp();
+                    convert_groups<2, 1>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane);
+                } else {
+                    store_final_groups(tmem + lanebase + kTmS, 0, 3, i, zrow, lane, rows_tab, s0h, s_outh,
+                                       z0h, z_outh);
+                }
+                __syncwarp();
             }
             if (!last) {
                 fence_async_smem();
@@ -639,16 +701,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_SB_FULL));
             }
+            if (tid == 384) LA_TR(TR_CONV, c, 1);
         }
     }
 
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
+        __syncwarp();  // lane 0 ran the producer loop alone; dealloc is warp-collective
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
 }
+
+#ifdef LA_TRACE
+}  // namespace
+extern "C" LA_API int la_debug_prefill_trace(void *host, size_t bytes) {
+    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+    return (int)cudaMemcpyFromSymbol(host, g_trace, bytes);
+}
+namespace {
+#endif
 
 using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                               const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
