@@ -204,7 +204,8 @@ la_status la_prefix_prefill(const void *q, const void *k, const void *v, const v
     pa.z_init = reinterpret_cast<float *>(ws + L.z_init);
     pa.status = status;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = la::launch_prefix_partials_simt(pa, dtype, cs);
+    cudaError_t e = dtype == LA_DTYPE_BF16 ? la::launch_prefix_partials_tc(pa, cs)
+                                           : la::launch_prefix_partials_simt(pa, dtype, cs);
     if (e == cudaSuccess) e = la::launch_prefix_reduce(pa, cs);
     if (e != cudaSuccess) return LA_ERR_CUDA;
     la::PrefillArgs a{q, k, v, pa.s_init, pa.z_init, y, s_out, z_out, B, H, N, eps, status};

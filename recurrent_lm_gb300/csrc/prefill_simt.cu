@@ -123,7 +123,7 @@ prefix_partial_simt_kernel(const T *__restrict__ ke, const T *__restrict__ ve,
     __shared__ float xk[kDFeat], vs[kDV];
     __shared__ float phk[kD];
     __shared__ float zsh[kD];
-    const int64_t seg = blockIdx.x, bh = blockIdx.y;
+    const int64_t bh = blockIdx.x, seg = blockIdx.y;
     const int tid = threadIdx.x;
     const int c = tid % kDV, g = tid / kDV;
     const int64_t j0 = seg * seg_len;
@@ -227,7 +227,8 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, la_dtype dt, cudaStream_t 
 }
 
 cudaError_t launch_prefix_partials_simt(const PrefixArgs &a, la_dtype dt, cudaStream_t st) {
-    dim3 grid((unsigned)a.nseg, (unsigned)(a.B * a.H));
+    if (a.nseg > 65535) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)(a.B * a.H), (unsigned)a.nseg);
     if (dt == LA_DTYPE_BF16)
         prefix_partial_simt_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
             (const __nv_bfloat16 *)a.k_e, (const __nv_bfloat16 *)a.v_e, a.M,

@@ -1,0 +1,197 @@
+// Prefix-state partial sums on the tensor cores (bf16 operands, fp32
+// accumulate): for each (b, h) and each segment of up to 2048 prefix tokens,
+//   s_E,seg = sum_j phi(k_e_j) v_e_j^T,   z_E,seg = sum_j phi(k_e_j)
+// ("Just read twice" reading notes, sec. 2.6: the non-causal encoder state of
+// prefix linear attention; sec. 2.8: the encoder state is accumulated first
+// and then seeds the causal scan).  A deterministic second pass adds the
+// segments in order (prefill_simt.cu), and the causal prefill starts from it.
+//
+// Same update as the causal prefill kernel: [S'^T ; z'] += [V | 1]^T Phi'_K
+// per 128-token chunk (8 MMAs of M = 128, N = 160, K = 16), with the compact
+// feature map generated one token per thread.  Splitting the prefix over
+// segments spreads the reduction over all SMs instead of lengthening each
+// (b, h) scan.  256 threads, about 108 KB of shared memory and 256 TMEM
+// columns per CTA, so two CTAs share an SM.
+#include "la_internal.h"
+#include "taylor_tc.cuh"
+#include "tc_common.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+using namespace taylor;
+
+constexpr int kC = 128;
+constexpr int kThreads = 256;
+constexpr int kStages = 2;
+
+// Shared memory map (bytes from a 1024-aligned base)
+constexpr uint32_t kSmPhiK = 0;        // MN-major B: 3 x 16K SW128
+constexpr uint32_t kSmV = 49152;       // 2 x [128][64] bf16 SW128
+constexpr uint32_t kSmOnes = 81920;    // [128][64] bf16 ones (rows 64..127 of [V | 1]^T)
+constexpr uint32_t kSmK = 98304;       // 2 x [128][16] bf16 SW32
+constexpr uint32_t kSmRows = 106496;   // [160] x int4 feature -> ABI row table
+constexpr uint32_t kSmBar = kSmRows + 160 * 16;
+constexpr uint32_t kSmTotal = kSmBar + 256;
+constexpr uint32_t kSmAlloc = kSmTotal + 1024;
+
+enum { B_KV_FULL = 0, B_KV_EMPTY = 2, B_PHK_FULL = 4, B_PHK_EMPTY, B_S_FULL, B_COUNT };
+constexpr uint32_t kSmTmemSlot = kSmBar + 8 * B_COUNT;
+constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
+static_assert(kSmAbort + 4 <= kSmTotal, "barrier area");
+
+constexpr uint32_t kIdUp = idesc_bf16(128, kNFeat, true, true);  // [V | 1]^T x Phi'_K
+
+__global__ void __launch_bounds__(kThreads, 2)
+prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                         int M, int seg_len, int nseg, float *__restrict__ part_s,
+                         float *__restrict__ part_z, unsigned *status) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    auto bar = [&](int i) { return sb + kSmBar + 8u * (uint32_t)i; };
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + kSmAbort);
+    const int4 *rows_tab = reinterpret_cast<const int4 *>(smem + kSmRows);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t bh = blockIdx.x;
+    const int seg = blockIdx.y;
+    const int j0 = seg * seg_len;
+    const int j1 = min(M, j0 + seg_len);
+    const int n = (j1 - j0 + kC - 1) / kC;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(B_KV_FULL + s), 1);
+            mbar_init(bar(B_KV_EMPTY + s), 1 + 4);
+        }
+        mbar_init(bar(B_PHK_FULL), 4);
+        mbar_init(bar(B_PHK_EMPTY), 1);
+        mbar_init(bar(B_S_FULL), 1);
+        *abort = 0;
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        tmem_alloc(sb + kSmTmemSlot, 256);
+        tmem_relinquish();
+    }
+    for (int i = tid; i < 16384 / 16; i += kThreads)
+        st_shared_v4(sb + kSmOnes + 16 * i, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    if (tid < kNFeat) {
+        const Rows r = abi_rows(tid);
+        reinterpret_cast<int4 *>(smem + kSmRows)[tid] = make_int4(r.r1, r.r2, r.kind, 0);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kSmTmemSlot);
+
+    if (warp == 0) {
+        // ================= TMA producer: k_e, v_e chunks of the segment =================
+        if (lane == 0) {
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            int issued = 0;
+            for (int c = 0; c < n; ++c) {
+                const int st = c % kStages;
+                if (!mbar_wait(bar(B_KV_EMPTY + st), ((uint32_t)(c / kStages) & 1u) ^ 1u, abort, status))
+                    break;
+                mbar_expect_tx(bar(B_KV_FULL + st), kC * 16 * 2 + kC * 64 * 2);
+                tma_load_3d(sb + kSmK + st * 4096, &tk, bar(B_KV_FULL + st), 0, j0 + c * kC, (int)bh);
+                tma_load_3d(sb + kSmV + st * 16384, &tv, bar(B_KV_FULL + st), 0, j0 + c * kC, (int)bh);
+                issued = c + 1;
+            }
+            if (*abort)
+                for (int c = (issued > kStages ? issued - kStages : 0); c < issued; ++c)
+                    drain_wait(bar(B_KV_FULL + c % kStages), (uint32_t)(c / kStages) & 1u);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer: [S'^T ; z'] += [V | 1]^T Phi'_K =================
+        if (lane == 0) {
+            const uint64_t dPhiK = smem_desc(sb + kSmPhiK, 16384, 1024, kSw128);
+            const uint64_t dV0 = smem_desc(sb + kSmV, kSmOnes - kSmV, 1024, kSw128);
+            bool ok = true;
+            for (int c = 0; c < n; ++c) {
+                const int st = c % kStages;
+                const uint64_t dV = dV0 + (uint64_t)(st * (16384 >> 4)) - ((uint64_t)(st * (16384 >> 4)) << 16);
+                ok = mbar_wait(bar(B_PHK_FULL), (uint32_t)c & 1u, abort, status) &&
+                     mbar_wait(bar(B_KV_FULL + st), (uint32_t)(c / kStages) & 1u, abort, status);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_bf16(tmem, dV + s * (2048 >> 4), dPhiK + s * (2048 >> 4), kIdUp, (c > 0 || s > 0));
+                mma_commit(bar(B_PHK_EMPTY));
+                mma_commit(bar(B_KV_EMPTY + st));
+            }
+            mma_commit(bar(B_S_FULL));  // also covers an early exit: every issued MMA completes first
+        }
+    } else if (warp >= 4) {
+        // ================= feature generation (one token per thread) =================
+        const int t = tid - 128;
+        for (int c = 0; c < n; ++c) {
+            const int st = c % kStages;
+            if (!mbar_wait(bar(B_KV_FULL + st), (uint32_t)(c / kStages) & 1u, abort, status)) break;
+            uint4 klo, khi;
+            load_row16_raw(sb + kSmK + st * 4096, t, klo, khi);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_KV_EMPTY + st));
+            if (!mbar_wait(bar(B_PHK_EMPTY), ((uint32_t)c & 1u) ^ 1u, abort, status)) break;
+            const bool pad = j0 + c * kC + t >= j1;  // outside this segment: no contribution
+            emit_features<true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PHK_FULL));
+        }
+        // ---- partial state of this segment in the ABI layout (value rows d: lanes
+        // 0..63 of warps 4, 5; the z' row: lane 64, warp 6)
+        if (warp < 7) {
+            const int w = warp - 4;
+            const bool zrow = (w == 2);
+            const bool ok = mbar_wait(bar(B_S_FULL), 0, abort, status);
+            __syncwarp();
+            tc_fence_after();
+            if (ok && n > 0) {
+                const int64_t slot = bh * nseg + seg;
+                store_final_groups(tmem + ((uint32_t)(32 * w) << 16), 0, kNFeat / 32, 32 * w + lane, zrow, lane,
+                                   rows_tab, nullptr, part_s + slot * kD * kDV, nullptr, part_z + slot * kD);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prefix_partials_tc(const PrefixArgs &a, cudaStream_t st) {
+    const int64_t BH = a.B * a.H;
+    if (a.M > (int64_t)0x7FFFFFFF - kC || a.nseg > 65535) return cudaErrorInvalidValue;
+    CUtensorMap tk, tv;
+    if (!make_row_tmap(&tk, a.k_e, BH, a.M, 16, false) || !make_row_tmap(&tv, a.v_e, BH, a.M, 64, true))
+        return cudaErrorInvalidValue;
+    static int configured_for = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_for != dev) {
+        cudaError_t e = cudaFuncSetAttribute(prefix_partial_tc_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+        if (e != cudaSuccess) return e;
+        configured_for = dev;
+    }
+    dim3 grid((unsigned)BH, (unsigned)a.nseg);
+    prefix_partial_tc_kernel<<<grid, kThreads, kSmAlloc, st>>>(tk, tv, (int)a.M, (int)a.seg_len,
+                                                               (int)a.nseg, a.part_s, a.part_z, a.status);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -60,7 +60,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // as soon as another role of the CTA has aborted.  The polling loop is kept
 // out of line so the many call sites stay small (instruction-cache pressure).
 constexpr long long kWaitCycles = 2000000000LL;  // about one second
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
                                             unsigned *status) {
     const long long t0 = clock64();
     while (true) {

@@ -157,3 +157,16 @@ def test_prefix_full_size_sampled_heads():
 def test_timeout_status_is_clear_after_normal_calls():
     la.prefill(*(t.to(DEV) for t in inputs.qkv(1, 1, 10, seed=1)[:3]))
     la.check_device_status()
+
+
+def test_prefix_bitwise_deterministic():
+    """The split-M prefix reduction sums segments in a fixed order: repeated
+    calls give identical bits (256 heads, 3 segments, non-zero s0)."""
+    q, k, v, ke, ve = inputs.qkv(16, 16, 2100, seed=77, M=5000 - 2900)
+    s0, z0 = inputs.random_state(16, 16, seed=78, tokens=512.0)
+    args = [t.to(DEV) for t in (q, k, v, ke, ve, s0, z0)]
+    first = la.prefix_prefill(*args)
+    again = la.prefix_prefill(*args)
+    torch.cuda.synchronize()
+    for x, y in zip(first, again):
+        assert torch.equal(x, y)
