@@ -65,7 +65,8 @@ constexpr uint32_t kSmV = 116736;      // 3 x [128][64] bf16 SW128
 constexpr uint32_t kSmOnes = 165888;   // [128][64] bf16 ones (the extra rows/columns of [V | 1])
 constexpr uint32_t kSmQ = 182272;      // 3 x [128][16] bf16 SW32
 constexpr uint32_t kSmK = 194560;      // 3 x [128][16] bf16 SW32
-constexpr uint32_t kSmRows = 206848;   // [160] x int4 feature -> ABI row table
+constexpr uint32_t kSmY = 206848;      // 4 x [32 rows][64] bf16 SW128: y staging for TMA stores
+constexpr uint32_t kSmRows = kSmY + 16384;  // [160] x int4 feature -> ABI row table
 constexpr uint32_t kSmBar = kSmRows + 160 * 16;
 constexpr uint32_t kSmTotal = kSmBar + 512;
 constexpr uint32_t kSmAlloc = kSmTotal + 1024;
@@ -83,7 +84,7 @@ constexpr uint32_t kSmTmemSlot = kSmBar + 8 * B_COUNT;
 constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
 static_assert(kSmAbort + 4 <= kSmTotal, "barrier area");
 static_assert(kSmSb + 25600 <= kSmV && kSmV + 3 * 16384 == kSmOnes && kSmOnes + 16384 == kSmQ &&
-              kSmQ + 3 * 4096 == kSmK && kSmK + 3 * 4096 == kSmRows, "smem map");
+              kSmQ + 3 * 4096 == kSmK && kSmK + 3 * 4096 == kSmY && kSmAlloc <= 232448, "smem map");
 
 constexpr uint32_t kIdQK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdPV = idesc_bf16(128, kNB, false, true);   // P (TMEM) x [V | 1]
@@ -145,7 +146,8 @@ enum { TR_TMA = 0, TR_MMA, TR_GEN, TR_EPI, TR_CONV };
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv, const float *__restrict__ s0,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty,
+                  const float *__restrict__ s0,
                   const float *__restrict__ z0, __nv_bfloat16 *__restrict__ y,
                   float *__restrict__ s_out, float *__restrict__ z_out, int N, float eps,
                   unsigned *status) {
@@ -482,20 +484,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_NUM_EMPTY));
-                const int row = c * kC + i;
-                if (row < N) {
-                    const float inv = 1.0f / (__uint_as_float(dr) + eps);
-                    const uint64_t inv2 = f2pack(inv, inv);
-                    uint4 *dst = reinterpret_cast<uint4 *>(y + ((int64_t)bh * N + row) * kDV);
+                // y rows of this warp -> its 4 KB staging tile -> one bulk tensor store
+                // (rows past N are clipped by the store)
+                const float inv = 1.0f / (__uint_as_float(dr) + eps);
+                const uint64_t inv2 = f2pack(inv, inv);
+                const uint32_t stage = sb + kSmY + (uint32_t)w * 4096;
+                if (lane == 0) bulk_wait_read0();  // previous chunk's store has read the tile
+                __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint32_t o[4];
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t o[4];
 #pragma unroll
-                        for (int h = 0; h < 4; ++h)
-                            o[h] = pack_bf16x2(fmul2((uint64_t)r[8 * j + 2 * h] | ((uint64_t)r[8 * j + 2 * h + 1] << 32),
-                                                     inv2));
-                        dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
+                    for (int h = 0; h < 4; ++h)
+                        o[h] = pack_bf16x2(fmul2((uint64_t)r[8 * j + 2 * h] | ((uint64_t)r[8 * j + 2 * h + 1] << 32),
+                                                 inv2));
+                    st_shared_v4(stage + lane * 128 + ((j ^ (lane & 7)) << 4), o[0], o[1], o[2], o[3]);
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0 && c * kC + 32 * w < N) {
+                    tma_store_3d(&ty, stage, 0, c * kC + 32 * w, (int)bh);
+                    bulk_commit();
                 }
             }
             if (tid == 384) LA_TR(TR_EPI, c, 3);
@@ -524,6 +533,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             if (tid == 384) LA_TR(TR_CONV, c, 1);
         }
+        if (lane == 0) bulk_wait0();  // y stores complete before the CTA exits
     }
 
     tc_fence_before();
@@ -567,12 +577,12 @@ EncodeFn encode_fn() {
 // [BH][N][width] bf16 rows as a 3-D tensor map with a {width, 128, 1} box;
 // rows past N read as zero.
 bool make_row_tmap(CUtensorMap *map, const void *base, int64_t BH, int64_t N, int width,
-                   bool swizzle128) {
+                   bool swizzle128, int box_rows) {
     EncodeFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)N, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)N * width * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)width, 128u, 1u};
+    const cuuint32_t box[3] = {(cuuint32_t)width, (cuuint32_t)box_rows, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -583,9 +593,9 @@ bool make_row_tmap(CUtensorMap *map, const void *base, int64_t BH, int64_t N, in
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     const int64_t BH = a.B * a.H;
     if (a.N > (int64_t)0x7FFFFFFF - kC) return cudaErrorInvalidValue;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, ty;
     if (!make_row_tmap(&tq, a.q, BH, a.N, 16, false) || !make_row_tmap(&tk, a.k, BH, a.N, 16, false) ||
-        !make_row_tmap(&tv, a.v, BH, a.N, 64, true))
+        !make_row_tmap(&tv, a.v, BH, a.N, 64, true) || !make_row_tmap(&ty, a.y, BH, a.N, 64, true, 32))
         return cudaErrorInvalidValue;
     static int configured_for = -1;
     int dev = 0;
@@ -597,7 +607,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
         configured_for = dev;
     }
     prefill_tc_kernel<<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-        tq, tk, tv, a.s0, a.z0, (__nv_bfloat16 *)a.y, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+        tq, tk, tv, ty, a.s0, a.z0, (__nv_bfloat16 *)a.y, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
     return cudaGetLastError();
 }
 

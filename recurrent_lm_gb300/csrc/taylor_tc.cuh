@@ -182,20 +182,39 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Final ABI state from TMEM rows, for one warp's lanes and feature groups
-// [g0, g0 + ng): value rows d < 64, and the z' row (lane 64, by lane 0 of the
-// warp that owns lanes 64..95).  Runs once per CTA, so it is kept out of line.
+// [g0, g0 + ng): value rows d < 64 (column d of each ABI row), and the z' row
+// (lane 64, by lane 0 of the warp that owns lanes 64..95).  Each group's reads
+// of the initial state are issued together before its stores.  Runs once per
+// CTA, so it is kept out of line.
 static __device__ __noinline__ void store_final_groups(uint32_t taddr, int g0, int ng, int d, bool zrow, int lane,
-                                                const int4 *rows_tab, const float *s0h, float *s_outh,
-                                                const float *z0h, float *z_outh) {
+                                                       const int4 *rows_tab, const float *s0h, float *s_outh,
+                                                       const float *z0h, float *z_outh) {
+    const float *col0 = zrow ? z0h : (s0h ? s0h + d : nullptr);
+    float *out = zrow ? z_outh : (s_outh ? s_outh + d : nullptr);
+    const int64_t stride = zrow ? 1 : kDV;
     for (int g = g0; g < g0 + ng; ++g) {
         uint32_t r[32];
         tmem_load32_sync(taddr + 32 * g, r);
-        if (!zrow || lane == 0) {
+        if (out && (!zrow || lane == 0)) {
+            float anti[32];
+#pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int4 e = rows_tab[32 * g + j];
-                if (zrow) store_compact(z0h, z_outh, 1, Rows{e.x, e.y, e.z}, __uint_as_float(r[j]));
-                else store_compact(s0h ? s0h + d : nullptr, s_outh ? s_outh + d : nullptr, kDV,
-                                   Rows{e.x, e.y, e.z}, __uint_as_float(r[j]));
+                anti[j] = (col0 && e.z == 1) ? 0.5f * (col0[e.x * stride] - col0[e.y * stride]) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int4 e = rows_tab[32 * g + j];
+                const float x = __uint_as_float(r[j]);
+                if (e.z == 2) {
+                    out[e.x * stride] = x;
+                } else if (e.z == 0) {
+                    out[e.x * stride] = x * kSqrt2;
+                } else if (e.z == 1) {
+                    const float sym = x * kRSqrt2;
+                    out[e.x * stride] = sym + anti[j];
+                    out[e.y * stride] = sym - anti[j];
+                }
             }
         }
         __syncwarp();

@@ -88,6 +88,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
         : "memory");
 }
+// Bulk tensor store from shared memory (rows past the tensor's extent are
+// clipped), tracked by the issuing thread's bulk-async group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until the group's shared-memory reads are done (the buffer may be reused)
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// wait until the group's writes are complete
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -312,6 +328,6 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 // [BH][N][width] bf16 rows as a 3-D TMA tensor map with a {width, 128, 1} box
 // (128-byte swizzle if swizzle128, else 32-byte); rows past N read as zero.
 bool make_row_tmap(CUtensorMap *map, const void *base, int64_t BH, int64_t N, int width,
-                   bool swizzle128);
+                   bool swizzle128, int box_rows = 128);
 
 }  // namespace la
