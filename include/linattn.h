@@ -64,7 +64,9 @@ typedef enum {
     LA_ERR_UNSUPPORTED = 2,   /* d_feat != 16, d_v != 64, unknown dtype, no sm_103 device */
     LA_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
     LA_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
-    LA_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (see la_check_device_status) */
+    LA_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up (see la_check_device_status) */
+    LA_ERR_SCRATCH_TOO_SMALL = 6  /* la_prefix_prefill_noalloc: the problem needs more scratch than
+                                     the library's fixed buffer holds (use la_prefix_prefill) */
 } la_status;
 
 typedef enum {
@@ -149,6 +151,42 @@ LA_API la_status la_decode_step(const void *q, const void *k, const void *v,
                          float *s_out, float *z_out, void *y,
                          int64_t B, int64_t H, int d_feat, int d_v,
                          la_dtype dtype, float eps, la_stream_t stream);
+
+/*
+ * la_prefix_prefill_noalloc -- the same computation as la_prefix_prefill, for
+ * callers that cannot allocate device memory when they call (for example a
+ * serving loop that must not trigger the device synchronisation an
+ * allocation implies, or a plug-in whose host process owns all device memory
+ * through its own allocator).  There is no counterpart on the pages; it
+ * exists only for such callers.
+ *
+ * Instead of a caller-provided workspace it uses one scratch buffer of
+ * la_noalloc_scratch_bytes() bytes (32 MiB) that the library reserves in
+ * device memory on every device where it is loaded, until the process exits.
+ *   - No memory is allocated by the call (no cudaMalloc, no allocating
+ *     library routine).  The caller still passes all inputs and outputs.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before capturing the stream into a CUDA graph.
+ *   - Problems with la_prefix_workspace_size(B, H, M) larger than the buffer
+ *     return LA_ERR_SCRATCH_TOO_SMALL before any work is queued; roughly
+ *     B*H*(ceil(M/2048) + 1) <= 472 fits.
+ *   - Every call on a device shares the buffer, and the buffer keeps the last
+ *     call's contents.  Nothing in it needs to start at zero (each call
+ *     writes every part it reads).  Calls whose work overlaps on the GPU (two
+ *     streams, or two threads) race on the buffer and give wrong results:
+ *     serialise them.
+ * All other arguments, layouts and errors are those of la_prefix_prefill.
+ */
+LA_API la_status la_prefix_prefill_noalloc(const void *q, const void *k, const void *v,
+                                           const void *k_e, const void *v_e, int64_t M,
+                                           const float *s0, const float *z0,
+                                           void *y, float *s_out, float *z_out,
+                                           int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                                           la_dtype dtype, float eps, la_stream_t stream);
+
+/* Size in bytes of the fixed scratch buffer used by la_prefix_prefill_noalloc. */
+LA_API size_t la_noalloc_scratch_bytes(void);
 
 /* Static English description of a status code (never NULL). */
 LA_API const char *la_status_string(la_status status);

@@ -18,7 +18,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblinattn.so")
 D_FEAT, D_V, D_PHI = 16, 64, 273
 
-LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(6)
+(LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED, LA_ERR_CUDA, LA_ERR_TIMEOUT,
+ LA_ERR_SCRATCH_TOO_SMALL) = range(7)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
 
 _lib = None
@@ -42,6 +43,9 @@ SIGNATURES = {
                                _SZ, _I64, _I64, _I64, _I, _I, _I, _F, _VP]),
     "la_decode_step": (_I, [_VP, _VP, _VP, _FP, _FP, _FP, _FP, _VP, _I64, _I64, _I, _I, _I,
                             _F, _VP]),
+    "la_prefix_prefill_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _FP, _FP,
+                                       _I64, _I64, _I64, _I, _I, _I, _F, _VP]),
+    "la_noalloc_scratch_bytes": (_SZ, []),
     "la_status_string": (ctypes.c_char_p, [_I]),
     "la_check_device_status": (_I, [_VP]),
     "la_version": (_I, []),
@@ -175,6 +179,40 @@ def prefix_prefill(q, k, v, k_e, v_e, s0=None, z0=None, *, eps: float = 0.0, y=N
         _ptr(s_out), _ptr(z_out), _ptr(workspace), workspace.numel(), B, H, N, D_FEAT, D_V,
         _dt(q), float(eps), _stream(stream)))
     return y, s_out, z_out
+
+
+def prefix_prefill_noalloc(q, k, v, k_e, v_e, s0=None, z0=None, *, eps: float = 0.0, y=None,
+                           s_out=None, z_out=None, want_state: bool = True, stream=None):
+    """la_prefix_prefill_noalloc: JRT-RNN prefix prefill for callers that cannot
+    allocate device memory when they call; the library's fixed scratch buffer
+    replaces the workspace (outputs are still allocated here when not given)."""
+    lib = load_library()
+    B, H, N, _ = q.shape
+    dt = q.dtype
+    M = k_e.shape[2]
+    _need(q, "q", (B, H, N, D_FEAT), dt)
+    _need(k, "k", (B, H, N, D_FEAT), dt)
+    _need(v, "v", (B, H, N, D_V), dt)
+    _need(k_e, "k_e", (B, H, M, D_FEAT), dt)
+    _need(v_e, "v_e", (B, H, M, D_V), dt)
+    if s0 is not None or z0 is not None:
+        _need(s0, "s0", (B, H, D_PHI, D_V), torch.float32)
+        _need(z0, "z0", (B, H, D_PHI), torch.float32)
+    if y is None:
+        y = torch.empty((B, H, N, D_V), dtype=dt, device=q.device)
+    if want_state:
+        if s_out is None:
+            s_out = torch.empty((B, H, D_PHI, D_V), dtype=torch.float32, device=q.device)
+        if z_out is None:
+            z_out = torch.empty((B, H, D_PHI), dtype=torch.float32, device=q.device)
+    _raise(lib.la_prefix_prefill_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_e), _ptr(v_e), M, _ptr(s0), _ptr(z0), _ptr(y),
+        _ptr(s_out), _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q), float(eps), _stream(stream)))
+    return y, s_out, z_out
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(load_library().la_noalloc_scratch_bytes())
 
 
 def decode_step(q, k, v, s, z, *, eps: float = 0.0, y=None, s_out=None, z_out=None,

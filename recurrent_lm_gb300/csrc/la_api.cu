@@ -125,6 +125,8 @@ const char *la_status_string(la_status s) {
         case LA_ERR_MISALIGNED: return "a buffer is not 16-byte aligned";
         case LA_ERR_CUDA: return "CUDA runtime error or kernel launch failure";
         case LA_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+        case LA_ERR_SCRATCH_TOO_SMALL:
+            return "problem needs more scratch than the no-allocation buffer holds (use la_prefix_prefill)";
     }
     return "unknown status";
 }
