@@ -110,15 +110,18 @@ def kernel_traffic(kernel: str):
     return rec["bytes_per_launch"] if sha == rec["source_sha"] else None
 
 
+TIMED_WINDOWS = []   # (start, end) wall-clock seconds of every timed region
+
+
 class Clocks:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of SM clock and throttle reasons; only samples taken
+    inside a timed region (TIMED_WINDOWS) are summarised."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, dev: int):
         self.proc = None
-        self.lines = []
         try:
             uuid = str(torch.cuda.get_device_properties(dev).uuid)
             self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
@@ -126,10 +129,13 @@ class Clocks:
             self.sel = []
 
     def start(self):
+        import tempfile
+        # samples go to a file: a pipe that nobody reads would fill and stall them
+        self.log = tempfile.TemporaryFile(mode="w+")
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", *self.sel, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=self.log, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
@@ -138,28 +144,50 @@ class Clocks:
             return None
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-            out = ""
-        mhz, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            self.proc.wait()
+        self.log.seek(0)
+        out = self.log.read()
+        self.log.close()
+        import datetime
+        rows = []
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
+            if len(f) < 9:
                 continue
             try:
-                mhz.append(float(f[0]))
-                mx = max(mx, float(f[1]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[1]), float(f[2]), f))
             except ValueError:
                 continue
-            for n, val in zip(names, f[4:8]):
+        # samples inside the timed regions; if the regions were too short to
+        # catch one, those between the first region's start and the last's end
+        inside = [r for r in rows if any(a <= r[0] <= b for a, b in TIMED_WINDOWS)]
+        scope = "timed regions"
+        if not inside and TIMED_WINDOWS:
+            lo, hi = min(a for a, _ in TIMED_WINDOWS), max(b for _, b in TIMED_WINDOWS)
+            inside = [r for r in rows if lo <= r[0] <= hi]
+            scope = "span of the timed regions"
+        mhz, watts, reasons = [], [], set()
+        mx = max((r[2] for r in rows), default=0.0)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, sm, _, f in inside:
+            mhz.append(sm)
+            try:
+                watts.append(float(f[3]))
+            except ValueError:
+                pass
+            for n, val in zip(names, f[5:9]):
                 if val.lower() == "active":
                     reasons.add(n)
         if not mhz:
-            return None
+            return {"sm_mhz": None, "sm_max_mhz": mx or None, "reasons": [],
+                    "samples": 0, "samples_total": len(rows)}
         return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(mhz)}
+                "samples": len(mhz), "samples_total": len(rows), "scope": scope,
+                "power_w_median": statistics.median(watts) if watts else None}
 
 
 def time_loop(fn, steps, warmup, dist):
@@ -173,14 +201,21 @@ def time_loop(fn, steps, warmup, dist):
     st = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
     e0.record(st)
     for _ in range(steps):
         fn()
     e1.record(st)
     e1.synchronize()
     torch.cuda.synchronize()
+    TIMED_WINDOWS.append((t0, time.time()))
     dist.barrier()
     return dist.max(e0.elapsed_time(e1) / steps)
+
+
+def shard_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling over independent heads)."""
+    return seed + 7919 * rank
 
 
 def gen_device(shape, gen, dtype=torch.bfloat16, dev="cuda"):
@@ -192,7 +227,7 @@ def leg_prefill(la, args, dist, dev, clocks):
     w = inputs.WORKLOADS[3]
     B, H, N = w.B, w.H, w.N
     g = torch.Generator(device=dev)
-    g.manual_seed(w.seed + 7919 * dist.rank)
+    g.manual_seed(shard_seed(w.seed, dist.rank))
     q = gen_device((B, H, N, 16), g, dev=dev)
     k = gen_device((B, H, N, 16), g, dev=dev)
     v = gen_device((B, H, N, 64), g, dev=dev)
@@ -208,11 +243,9 @@ def leg_prefill(la, args, dist, dev, clocks):
     def step():
         la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z)
 
-    clocks.start()
     ms = time_loop(step, args.steps, args.warmup, dist)
-    clk = clocks.stop()
     la.check_device_status()
-    out = {"ms": ms, "B": B, "H": H, "N": N, "clocks": clk,
+    out = {"ms": ms, "B": B, "H": H, "N": N,
            "finite": bool(torch.isfinite(y[:, :, -1].float()).all().item())}
     if not args.no_e2e:
         out["e2e"] = e2e_prefill(la, args, dist, q, k, v, s0, z0)
@@ -251,7 +284,7 @@ def leg_prefix(la, args, dist, dev):
     w = inputs.WORKLOADS[4]
     B, H, N, M = w.B, w.H, w.N, w.M
     g = torch.Generator(device=dev)
-    g.manual_seed(w.seed + 7919 * dist.rank)
+    g.manual_seed(shard_seed(w.seed, dist.rank))
     q = gen_device((B, H, N, 16), g, dev=dev)
     k = gen_device((B, H, N, 16), g, dev=dev)
     v = gen_device((B, H, N, 64), g, dev=dev)
@@ -274,7 +307,7 @@ def leg_decode(la, args, dist, dev):
     w = inputs.WORKLOADS[5]
     B, H, T = w.B, w.H, args.decode_steps
     g = torch.Generator(device=dev)
-    g.manual_seed(w.seed + 7919 * dist.rank)
+    g.manual_seed(shard_seed(w.seed, dist.rank))
     qs = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
     ks = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
     vs = gen_device((B, H, w.s0_tokens, 64), g, dev=dev)
@@ -321,12 +354,12 @@ def cpu_baseline_prefill(sample_rows: int):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs", default="prefill,prefix,decode")
     ap.add_argument("--decode-steps", type=int, default=512)
-    ap.add_argument("--cpu-sample-rows", type=int, default=4)
+    ap.add_argument("--cpu-sample-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -344,12 +377,14 @@ def main():
     pk = peaks()
     clocks = Clocks(dist.local)
 
+    clocks.start()  # sampled across every timed leg
     pre = leg_prefill(la, args, dist, dev, clocks)
     res = {}
     if "prefix" in legs:
         res["prefix"] = leg_prefix(la, args, dist, dev)
     if "decode" in legs:
         res["decode"] = leg_decode(la, args, dist, dev)
+    pre["clocks"] = clocks.stop()
 
     W = dist.world
     tokens = pre["B"] * pre["N"]
@@ -386,6 +421,7 @@ def main():
                      "hbm_frac": hbm_gbs / pk["hbm_gbs"], "algorithmic_bytes_per_launch": nbytes},
         "gpu_launches": args.steps,
         "clocks": pre["clocks"],
+        "clocks_note": "nvidia-smi samples every 100 ms inside the timed regions of all legs",
         "legs": {},
     }
     if "e2e" in pre:

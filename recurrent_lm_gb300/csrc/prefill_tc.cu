@@ -76,9 +76,9 @@ constexpr int kStages = 3;
 enum {
     B_QK_FULL = 0, B_QK_EMPTY = 3, B_V_FULL = 6, B_V_EMPTY = 9,
     B_T_FULL = 12,   // [2] per T buffer
-    B_PV_DONE = 14,  // [2] per T buffer: P V of that buffer completed
-    B_P_FULL = 16, B_PHQ_FULL, B_PHQ_EMPTY, B_PHK_FULL, B_PHK_EMPTY,
-    B_NUM_FULL, B_NUM_EMPTY, B_S_FULL, B_SB_FULL, B_FINAL, B_COUNT
+    B_P_FULL = 14, B_PHQ_FULL, B_PHK_FULL,
+    B_NUM_FULL, B_NUM_EMPTY, B_S_FULL, B_SB_FULL, B_FINAL,
+    B_COUNT
 };
 constexpr uint32_t kSmTmemSlot = kSmBar + 8 * B_COUNT;
 constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
@@ -175,19 +175,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(B_QK_FULL + s), 1);
-            mbar_init(bar(B_QK_EMPTY + s), 1 + 4);
+            mbar_init(bar(B_QK_EMPTY + s), 4 + 1);  // gen warps read q, k; Q K^T of the chunk completed
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_T_FULL + i), 1);
-            mbar_init(bar(B_PV_DONE + i), 1);
         }
         mbar_init(bar(B_P_FULL), 4);
         mbar_init(bar(B_PHQ_FULL), 4);
-        mbar_init(bar(B_PHQ_EMPTY), 1);
         mbar_init(bar(B_PHK_FULL), 4);
-        mbar_init(bar(B_PHK_EMPTY), 1);
         mbar_init(bar(B_NUM_FULL), 1);
         mbar_init(bar(B_NUM_EMPTY), 4);
         mbar_init(bar(B_S_FULL), 1);
@@ -224,17 +221,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int d = 32 * w + lane;
         const bool zrow = (w == 2);
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
+        const float *col0 = zrow ? z0h : (s0h ? s0h + d : nullptr);
+        const int stride = zrow ? 1 : kDV;
 #pragma unroll 1
         for (int g = 0; g < kNFeat / 32; ++g) {
             uint32_t r[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int4 e = rows_tab[32 * g + j];
-                const Rows rw{e.x, e.y, e.z};
-                const float x = zrow ? compact_initial(z0h, 1, rw)
-                                     : compact_initial(s0h ? s0h + d : nullptr, kDV, rw);
-                r[j] = __float_as_uint(x);
-            }
+            compact_initial_group(col0, stride, rows_tab + 32 * g, r);
             __syncwarp();
             tmem_store32_sync(tmem + lanebase + kTmS + 32 * g, r);
             if (!zrow || lane == 0) write_sb_group(sb + kSmSb, zrow ? 64 : d, g, r);
@@ -296,8 +288,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             auto issue_qk = [&](int c) {  // T[c & 1] = Q_c K_c^T
                 const int st = c % kStages;
                 mma_bf16(tmem + tm_t(c & 1), dQ + st * (4096 >> 4), dK + st * (4096 >> 4), kIdQK, 0);
-                mma_commit(bar(B_T_FULL + (c & 1)));
-                mma_commit(bar(B_QK_EMPTY + st));
+                mma_commit(bar(B_T_FULL + (c & 1)));  // also frees the q, k stage (P epilogue forwards it)
             };
             bool ok = mbar_wait(bar(B_QK_FULL + 0), 0, abort, status);
             if (ok) {
@@ -308,35 +299,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 const int vs = c % kStages, b = c & 1;
                 const uint64_t dV = dVst(vs);
                 const uint32_t pc = (uint32_t)c & 1u;
-                // P(c) is in T[b]; V(c) is in; num was drained for chunk c - 1
+                // P(c) is in T[b]; V(c) is in; num was drained for chunk c - 1 (which
+                // also means P V of chunk c - 1 completed: the read-out commit covers
+                // every earlier MMA, so T[b ^ 1] may take Q K^T(c + 1)); q, k of c + 1
                 ok = mbar_wait(bar(B_P_FULL), pc, abort, status) &&
                      mbar_wait(bar(B_V_FULL + vs), (uint32_t)(c / kStages) & 1u, abort, status) &&
-                     mbar_wait(bar(B_NUM_EMPTY), pc ^ 1u, abort, status);
+                     mbar_wait(bar(B_NUM_EMPTY), pc ^ 1u, abort, status) &&
+                     (c + 1 >= n || mbar_wait(bar(B_QK_FULL + (c + 1) % kStages),
+                                              (uint32_t)((c + 1) / kStages) & 1u, abort, status));
                 if (!ok) break;
                 LA_TR(TR_MMA, c, 0);
                 tc_fence_after();
-                // next chunk's Q K^T into the other T buffer, once P V of chunk c - 1 left it
-                if (c + 1 < n) {
-                    ok = mbar_wait(bar(B_QK_FULL + (c + 1) % kStages), (uint32_t)((c + 1) / kStages) & 1u,
-                                   abort, status) &&
-                         (c == 0 || mbar_wait(bar(B_PV_DONE + (b ^ 1)), (uint32_t)((c - 1) >> 1) & 1u,
-                                              abort, status));
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_qk(c + 1);
-                }
+                if (c + 1 < n) issue_qk(c + 1);
                 LA_TR(TR_MMA, c, 1);
                 // intra-chunk: [num | den] = P [V | 1], P from TMEM
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
                     mma_bf16_ts(tmem + kTmNum, tmem + tm_t(b) + 8 * s, dV + s * (2048 >> 4), kIdPV, s > 0);
-                mma_commit(bar(B_PV_DONE + b));
-                // inter-chunk read-out: [num | den] += Phi'_Q [S' | z'] (both K-major)
-                ok = mbar_wait(bar(B_SB_FULL), pc, abort, status) &&
-                     mbar_wait(bar(B_PHQ_FULL), pc, abort, status);
+                // inter-chunk read-out operands: the state after chunk c - 1, Phi'_Q(c)
+                ok = mbar_wait(bar(B_SB_FULL), pc, abort, status) && mbar_wait(bar(B_PHQ_FULL), pc, abort, status);
                 if (!ok) break;
                 LA_TR(TR_MMA, c, 2);
                 tc_fence_after();
+                // inter-chunk read-out: [num | den] += Phi'_Q [S' | z'] (both K-major)
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t o = (uint32_t)((s >> 2) * 16384 + (s & 3) * 32) >> 4;
@@ -346,25 +331,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                 for (int s = 8; s < 10; ++s)
                     mma_bf16(tmem + kTmNum, dPhiQ2 + ((s - 8) * 32 >> 4), dSb2 + ((s - 8) * 32 >> 4), kIdRO, 1);
-                mma_commit(bar(B_NUM_FULL));
-                mma_commit(bar(B_PHQ_EMPTY));
-                // state update: [S'^T ; z'] += [V | 1]^T Phi'_K, 16 tokens per MMA
-                ok = mbar_wait(bar(B_PHK_FULL), pc, abort, status);
-                if (!ok) break;
+                mma_commit(bar(B_NUM_FULL));  // also: Phi'_Q buffer free
+                // state update operand Phi'_K(c)
+                if (!(ok = mbar_wait(bar(B_PHK_FULL), pc, abort, status))) break;
                 LA_TR(TR_MMA, c, 3);
                 tc_fence_after();
+                // state update: [S'^T ; z'] += [V | 1]^T Phi'_K, 16 tokens per MMA
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
                     mma_bf16(tmem + kTmS, dV + s * (2048 >> 4), dPhiK + s * (2048 >> 4), kIdUp, 1);
-                mma_commit(bar(B_S_FULL));
-                mma_commit(bar(B_PHK_EMPTY));
-                mma_commit(bar(B_V_EMPTY + vs));
+                mma_commit(bar(B_S_FULL));  // also: Phi'_K and V(c) buffers free (gen forwards the latter)
                 LA_TR(TR_MMA, c, 4);
             }
             // every issued MMA must finish before TMEM is released
             mma_commit(bar(B_FINAL));
             drain_wait(bar(B_FINAL), 0);
         }
+#ifdef LA_TRACE
+    } else if (warp == 3) {
+        // timeline only: completion times of each chunk's MMA groups (observed, not consumed)
+        if (lane == 0 && blockIdx.x == 0) {
+            for (int c = 0; c < n; ++c) {
+                if (c + 1 < n && !mbar_wait(bar(B_T_FULL + ((c + 1) & 1)), (uint32_t)((c + 1) >> 1) & 1u, abort, status)) break;
+                LA_TR(TR_TMA, c, 2);
+                if (!mbar_wait(bar(B_NUM_FULL), (uint32_t)c & 1u, abort, status)) break;
+                LA_TR(TR_TMA, c, 4);
+                if (!mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status)) break;
+                LA_TR(TR_TMA, c, 5);
+            }
+        }
+#endif
     } else if (warp >= 4 && warp < 8) {
         // ================= feature generation (one token per thread) =================
         const int t = tid - 128;
@@ -378,14 +374,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             load_row16_raw(sb + kSmK + st * 4096, t, klo, khi);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_QK_EMPTY + st));
-            if (!mbar_wait(bar(B_PHQ_EMPTY), pc ^ 1u, abort, status)) break;
+            // the read-out of chunk c - 1 (NUM_FULL) released the Phi'_Q buffer
+            if (!mbar_wait(bar(B_NUM_FULL), pc ^ 1u, abort, status)) break;
             emit_features<false>(qlo, qhi, sb + kSmPhiQ, t, false, std::make_integer_sequence<int, 20>{});
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PHQ_FULL));
             if (tid == 128) LA_TR(TR_GEN, c, 1);
             const bool pad = c * kC + t >= N;  // past the end: no contribution to S', z'
-            if (!mbar_wait(bar(B_PHK_EMPTY), pc ^ 1u, abort, status)) break;
+            // the update of chunk c - 1 (S_FULL) released the Phi'_K buffer and V(c - 1)
+            if (!mbar_wait(bar(B_S_FULL), pc ^ 1u, abort, status)) break;
+            if (c > 0 && tid == 128) mbar_arrive(bar(B_V_EMPTY + (c - 1) % kStages));
             if (tid == 128) LA_TR(TR_GEN, c, 2);
             emit_features<true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
             fence_async_smem();
@@ -402,6 +401,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         auto do_p = [&](int c) -> bool {
             const int b = c & 1;
             if (!mbar_wait(bar(B_T_FULL + b), (uint32_t)(c >> 1) & 1u, abort, status)) return false;
+            if (tid == 256) mbar_arrive(bar(B_QK_EMPTY + c % kStages));  // Q K^T(c) has read its q, k stage
             if (tid == 256 + 96) LA_TR(TR_EPI, c, 0);
             __syncwarp();  // tcgen05.ld/st below are warp-collective (.sync.aligned)
             tc_fence_after();

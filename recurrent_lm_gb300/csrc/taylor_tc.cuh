@@ -151,27 +151,37 @@ __device__ __forceinline__ Rows abi_rows(int f) {
     return {-1, -1, 3};
 }
 
-// Compact entry of the initial state for feature row f (r = its ABI rows):
-// squares carry 1/sqrt2, pairs the symmetric sum over (a,b) and (b,a).
-__device__ __forceinline__ float compact_initial(const float *col, int stride, const Rows &r) {
-    if (!col || r.kind == 3) return 0.f;
-    const float a = col[(int64_t)r.r1 * stride];
-    if (r.kind == 2) return a;
-    if (r.kind == 0) return a * kRSqrt2;
-    return (a + col[(int64_t)r.r2 * stride]) * kRSqrt2;
-}
-
-// Final ABI entries from compact value x: squares sqrt2 x; pairs x/sqrt2 plus
-// and minus half the antisymmetric part of the initial state.
-__device__ __forceinline__ void store_compact(const float *col0, float *out, int stride,
-                                              const Rows &r, float x) {
-    if (!out || r.kind == 3) return;
-    if (r.kind == 2) { out[(int64_t)r.r1 * stride] = x; return; }
-    if (r.kind == 0) { out[(int64_t)r.r1 * stride] = x * kSqrt2; return; }
-    const float sym = x * kRSqrt2;
-    const float anti = col0 ? 0.5f * (col0[(int64_t)r.r1 * stride] - col0[(int64_t)r.r2 * stride]) : 0.f;
-    out[(int64_t)r.r1 * stride] = sym + anti;
-    out[(int64_t)r.r2 * stride] = sym - anti;
+// Compact entries of the initial state for the 32 features of one row group
+// (rows table entries e[0..31]): squares carry 1/sqrt2, pairs the symmetric
+// sum over (a,b) and (b,a) times 1/sqrt2.  The loads are unconditional
+// (padding reads row 0, unpaired features read their row twice) and all issued
+// before any is used, so each half's 32 reads are in flight together instead of
+// paying one DRAM latency each.
+__device__ __forceinline__ void compact_initial_group(const float *col, int stride, const int4 *e,
+                                                      uint32_t (&r)[32]) {
+    if (!col) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = 0u;
+        return;
+    }
+#pragma unroll
+    for (int h = 0; h < 32; h += 16) {  // two halves of 16 features: fewer live registers
+        float a[16], b[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int4 t = e[h + j];
+            const int r1 = t.z == 3 ? 0 : t.x;
+            const int r2 = t.z == 1 ? t.y : r1;
+            a[j] = __ldg(col + (int64_t)r1 * stride);
+            b[j] = __ldg(col + (int64_t)r2 * stride);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int k = e[h + j].z;
+            const float x = k == 3 ? 0.f : k == 2 ? a[j] : k == 0 ? a[j] * kRSqrt2 : (a[j] + b[j]) * kRSqrt2;
+            r[h + j] = __float_as_uint(x);
+        }
+    }
 }
 
 // Drain wait used when unwinding: bounded, ignores the abort flag.
@@ -196,11 +206,23 @@ static __device__ __noinline__ void store_final_groups(uint32_t taddr, int g0, i
         uint32_t r[32];
         tmem_load32_sync(taddr + 32 * g, r);
         if (out && (!zrow || lane == 0)) {
+            // antisymmetric part of the initial state for the pairs: unconditional
+            // loads (other features read row 0 and discard it) so all are in flight at once
             float anti[32];
+            if (col0) {
+                float a[32], b[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int4 e = rows_tab[32 * g + j];
-                anti[j] = (col0 && e.z == 1) ? 0.5f * (col0[e.x * stride] - col0[e.y * stride]) : 0.f;
+                for (int j = 0; j < 32; ++j) {
+                    const int4 e = rows_tab[32 * g + j];
+                    const int r1 = e.z == 1 ? e.x : 0, r2 = e.z == 1 ? e.y : 0;
+                    a[j] = __ldg(col0 + r1 * stride);
+                    b[j] = __ldg(col0 + r2 * stride);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) anti[j] = rows_tab[32 * g + j].z == 1 ? 0.5f * (a[j] - b[j]) : 0.f;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) anti[j] = 0.f;
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
