@@ -93,20 +93,28 @@ def peaks():
             "source": "fallback"}
 
 
+def source_sha(paths) -> str:
+    """Hash of the kernel's source files (relative to the repository root)."""
+    h = hashlib.sha256()
+    for rel in paths:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch from a committed ncu capture, if the capture was
     taken on the current kernel source (profiles/traffic.json records a hash
-    of the source file); None otherwise."""
+    of the source files); None otherwise."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(kernel)
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src):
+    try:
+        sha = source_sha(rec["sources"])
+    except OSError:
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     return rec["bytes_per_launch"] if sha == rec["source_sha"] else None
 
 
@@ -350,6 +358,51 @@ def cpu_baseline_prefill(sample_rows: int):
                       f"({sample_rows * w.H * w.N} head-tokens, fp64, {dt:.1f} s)"}
 
 
+# ------------------------------------------------------------------ ncu cases
+def ncu_case(la, case: str):
+    """Small launches for ncu captures (a few GB on the device at most, inputs
+    still larger than L2): prefill B=16, H=16 at N=4096 then N=8192 with an
+    initial state, two launches each (DRAM traffic is linear in N, so the
+    full-length launch is extrapolated from the two sizes); decode at the bench
+    batch B=128, H=16, four steps in place; prefix N=M=4096, three calls."""
+    dev = "cuda:0"
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    if case == "prefill":
+        B, H = 16, 16
+        s0 = torch.randn(B, H, 273, 64, device=dev, generator=g)
+        z0 = torch.rand(B, H, 273, device=dev, generator=g) + 100.0
+        for N in (4096, 8192):
+            q = gen_device((B, H, N, 16), g, dev=dev)
+            k = gen_device((B, H, N, 16), g, dev=dev)
+            v = gen_device((B, H, N, 64), g, dev=dev)
+            for _ in range(2):
+                la.prefill(q, k, v, s0, z0)
+            torch.cuda.synchronize()
+            del q, k, v
+    elif case == "decode":
+        B, H = 128, 16
+        s = torch.randn(B, H, 273, 64, device=dev, generator=g)
+        z = torch.rand(B, H, 273, device=dev, generator=g) + 100.0
+        for _ in range(4):
+            q = gen_device((B, H, 16), g, dev=dev)
+            k = gen_device((B, H, 16), g, dev=dev)
+            v = gen_device((B, H, 64), g, dev=dev)
+            la.decode_step(q, k, v, s, z, inplace=True)
+    elif case == "prefix":
+        B, H, N, M = 16, 16, 4096, 4096
+        q, k = gen_device((B, H, N, 16), g, dev=dev), gen_device((B, H, N, 16), g, dev=dev)
+        v = gen_device((B, H, N, 64), g, dev=dev)
+        ke, ve = gen_device((B, H, M, 16), g, dev=dev), gen_device((B, H, M, 64), g, dev=dev)
+        for _ in range(3):
+            la.prefix_prefill(q, k, v, ke, ve)
+    else:
+        raise SystemExit(f"unknown ncu case {case}")
+    torch.cuda.synchronize()
+    la.check_device_status()
+    log(f"ncu case {case}: ok")
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -362,12 +415,18 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "prefix"],
+                    help="run one small case for an ncu capture and exit (no timing)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     dist = Dist()
     if args.impl == "reference":
         return main_reference(args, dist)
 
+    if args.ncu_case:
+        import recurrent_lm_gb300 as la
+        la.load_library()
+        return ncu_case(la, args.ncu_case)
     dist.init("nccl")
     dev = f"cuda:{dist.local}"
     torch.cuda.set_device(dev)
