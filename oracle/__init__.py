@@ -76,6 +76,10 @@ def _load():
         lib.oracle_prefix_prefill.argtypes = [P, P, P, P, P, L, P, P, P, P, P,
                                               L, L, L, L, L, D, I]
         lib.oracle_prefix_prefill.restype = I
+        LP = ctypes.POINTER(ctypes.c_long)
+        lib.oracle_prefix_prefill_padded.argtypes = [P, P, P, P, P, L, P, P, LP, P, P, P,
+                                                     L, L, L, L, L, D, I]
+        lib.oracle_prefix_prefill_padded.restype = I
         lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, P, P, L, L, L, L, D, I]
         lib.oracle_decode_step.restype = I
         lib.oracle_prefill_chunked.argtypes = [P, P, P, P, P, P, P, P, L, L, L, L,
@@ -131,8 +135,9 @@ def _check(rc):
 
 
 def prefix_prefill(q, k, v, ke=None, ve=None, s0=None, z0=None, eps=0.0,
-                   nthreads: int = 0):
+                   nthreads: int = 0, left_pad=None):
     """Prefix linear attention; ke/ve [B,H,M,*] (None: plain causal).
+    left_pad: per-batch-row count of leading padding positions (None: none).
     Returns (y [B,H,N,dv], s [B,H,D,dv], z [B,H,D]) in float64."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     ke, ve, s0, z0 = _f64(ke), _f64(ve), _f64(s0), _f64(z0)
@@ -149,15 +154,20 @@ def prefix_prefill(q, k, v, ke=None, ve=None, s0=None, z0=None, eps=0.0,
     y = np.empty((B, H, N, dv), dtype=np.float64)
     s = np.empty((B, H, D, dv), dtype=np.float64)
     z = np.empty((B, H, D), dtype=np.float64)
-    _check(_load().oracle_prefix_prefill(
+    lp = None
+    if left_pad is not None:
+        lp = np.ascontiguousarray(np.asarray(left_pad, dtype=np.int64).reshape(B))
+        assert ctypes.sizeof(ctypes.c_long) == 8
+    _check(_load().oracle_prefix_prefill_padded(
         _ptr(q), _ptr(k), _ptr(v), _ptr(ke), _ptr(ve), M, _ptr(s0), _ptr(z0),
+        None if lp is None else lp.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
         _ptr(y), _ptr(s), _ptr(z), B, H, N, dk, dv, float(eps), int(nthreads)))
     return y, s, z
 
 
-def prefill(q, k, v, s0=None, z0=None, eps=0.0, nthreads: int = 0):
+def prefill(q, k, v, s0=None, z0=None, eps=0.0, nthreads: int = 0, left_pad=None):
     """Causal prefill from an optional initial state; returns (y, s, z)."""
-    return prefix_prefill(q, k, v, None, None, s0, z0, eps, nthreads)
+    return prefix_prefill(q, k, v, None, None, s0, z0, eps, nthreads, left_pad=left_pad)
 
 
 def prefill_chunked(q, k, v, C: int, s0=None, z0=None, eps=0.0, nthreads: int = 0):

@@ -22,6 +22,10 @@
  *    (reading notes), sec. 2.6, Eqs. (3)-(4): prefix linear attention, a
  *    non-causal state s_E, z_E over the first M positions of a second K/V
  *    set, added to the causal state for every output position.
+ *  - same page, sec. 2.7 (inference with prompts shorter than M: left-pad to M
+ *    and mask the padding in the prefix linear attention) and sec. 4.7 (the
+ *    padding must be kept out of the linear-attention state): the padded
+ *    variants below drop the first p_b positions of row b from every sum.
  *  - "Understanding and Improving Length Generalization in Recurrent Models"
  *    (reading notes), sec. 2.5 "non-zero initial state", Eq. (4): with the
  *    identity transition the initial state simply adds to the running sum.
@@ -116,14 +120,21 @@ int oracle_max_threads(void) {
  *   s_E = sum_{j<=M} phi(ke_j) ve_j^T,   z_E = sum_{j<=M} phi(ke_j),
  *   y_i = phi(q_i)(s0 + s_E + s_{D,i}) / phi(q_i)(z0 + z_E + z_{D,i}).
  * M = 0 (or ke == NULL) is plain causal linear attention from (s0, z0).
- * The returned state is s0 + s_E + s_{D,N} (the merge of Eq. (4)). */
-int oracle_prefix_prefill(const double *q, const double *k, const double *v,
-                          const double *ke, const double *ve, long M,
-                          const double *s0, const double *z0, double *y,
-                          double *s_out, double *z_out, long B, long H, long N,
-                          long dk, long dv, double eps, int nthreads) {
+ * The returned state is s0 + s_E + s_{D,N} (the merge of Eq. (4)).
+ *
+ * Left padding (same page, sec. 2.7 and 4.7): with left_pad != NULL, row b's
+ * first p = left_pad[b] positions (0 <= p <= N) are padding.  Prefix
+ * positions j < min(p, M) and causal positions i < p are left out of every
+ * sum, and y_i = 0 for i < p.  left_pad == NULL means no padding. */
+int oracle_prefix_prefill_padded(const double *q, const double *k, const double *v,
+                                 const double *ke, const double *ve, long M,
+                                 const double *s0, const double *z0, const long *left_pad,
+                                 double *y, double *s_out, double *z_out, long B, long H,
+                                 long N, long dk, long dv, double eps, int nthreads) {
     if (dk < 1 || dk > 256 || dv < 1 || B < 0 || H < 0 || N < 0 || M < 0)
         return 1;
+    for (long b = 0; left_pad && b < B; ++b)
+        if (left_pad[b] < 0 || left_pad[b] > N) return 1;
     const long D = oracle_feature_dim(dk);
     set_threads(nthreads);
     int err = 0;
@@ -139,9 +150,10 @@ int oracle_prefix_prefill(const double *q, const double *k, const double *v,
         } else {
 #pragma omp for schedule(dynamic, 1)
             for (long bh = 0; bh < B * H; ++bh) {
+                const long pad = left_pad ? left_pad[bh / H] : 0;
                 load_state(s0, z0, bh, D, dv, s, z);
                 /* non-causal prefix state over the second K/V set */
-                for (long j = 0; ke && j < M; ++j) {
+                for (long j = pad < M ? pad : M; ke && j < M; ++j) {
                     oracle_phi(ke + (bh * M + j) * dk, dk, phk);
                     const double *vj = ve + (bh * M + j) * dv;
                     for (long f = 0; f < D; ++f) {
@@ -149,9 +161,13 @@ int oracle_prefix_prefill(const double *q, const double *k, const double *v,
                         z[f] += phk[f];
                     }
                 }
-                /* causal path over all N positions */
+                /* causal path over all N positions (padding: y = 0, no state change) */
                 for (long i = 0; i < N; ++i) {
                     const long t = bh * N + i;
+                    if (i < pad) {
+                        for (long c = 0; c < dv; ++c) y[t * dv + c] = 0.0;
+                        continue;
+                    }
                     step(q + t * dk, k + t * dk, v + t * dv, s, z, y + t * dv,
                          dk, dv, eps, phq, phk);
                 }
@@ -161,6 +177,15 @@ int oracle_prefix_prefill(const double *q, const double *k, const double *v,
         free(s); free(z); free(phq); free(phk);
     }
     return err;
+}
+
+int oracle_prefix_prefill(const double *q, const double *k, const double *v,
+                          const double *ke, const double *ve, long M,
+                          const double *s0, const double *z0, double *y,
+                          double *s_out, double *z_out, long B, long H, long N,
+                          long dk, long dv, double eps, int nthreads) {
+    return oracle_prefix_prefill_padded(q, k, v, ke, ve, M, s0, z0, NULL, y, s_out, z_out,
+                                        B, H, N, dk, dv, eps, nthreads);
 }
 
 /* Causal prefill from an optional initial state (BASED page Eqs. (1)-(3);

@@ -285,3 +285,67 @@ def test_cost_ratio_prefix_vs_causal():
     ratio = (N * per_token + M * per_prefix_token) / (N * per_token)
     assert ratio == pytest.approx(1.25)
     assert per_token == 70980
+
+
+# ---------------------------------------------------------------- left padding
+def _padded_case(M, N, pads, seed_scale=1.0):
+    B = len(pads)
+    q = rnd(B, 2, N, 16); k = rnd(B, 2, N, 16); v = rnd(B, 2, N, 8)
+    ke = rnd(B, 2, M, 16) if M else None
+    ve = rnd(B, 2, M, 8) if M else None
+    return q, k, v, ke, ve
+
+
+def test_left_padding_against_closed_form_on_the_valid_suffix():
+    """JRT sec. 2.7 and 4.7: a prompt shorter than M is left-padded and the
+    padding is kept out of the prefix linear-attention state (and out of the
+    causal state).  So row b with p_b padding positions gives, at every valid
+    position, the kernel closed form over its valid tokens alone: prefix keys
+    j in [p_b, M) and causal keys j in [p_b, i]; padded outputs are zero."""
+    M, N, pads = 13, 21, [0, 5, 13, 17]
+    q, k, v, ke, ve = _padded_case(M, N, pads)
+    y, _, _ = oracle.prefix_prefill(q, k, v, ke, ve, left_pad=pads)
+    for b, p in enumerate(pads):
+        pe = min(p, M)
+        ref = quadratic.prefix_closed_form(q[b:b + 1, :, p:], k[b:b + 1, :, p:], v[b:b + 1, :, p:],
+                                           ke[b:b + 1, :, pe:] if pe < M else None,
+                                           ve[b:b + 1, :, pe:] if pe < M else None)
+        assert rel(y[b:b + 1, :, p:], ref) < 1e-12, b
+        assert np.all(y[b, :, :p] == 0.0)
+
+
+def test_left_padding_state_is_the_valid_tokens_state():
+    """JRT sec. 2.6 Eq. (4) with the padding masked: the final state is
+    s0 + (sum over valid prefix tokens) + (sum over valid causal tokens),
+    i.e. what plain prefills of the valid tokens alone accumulate."""
+    M, N, pads = 9, 15, [3, 0, 15]
+    q, k, v, ke, ve = _padded_case(M, N, pads)
+    s0 = rnd(3, 2, 273, 8); z0 = np.abs(rnd(3, 2, 273)) + 1.0
+    _, s, z = oracle.prefix_prefill(q, k, v, ke, ve, s0, z0, left_pad=pads)
+    for b, p in enumerate(pads):
+        pe = min(p, M)
+        sE = np.zeros((1, 2, 273, 8)); zE = np.zeros((1, 2, 273))
+        if pe < M:
+            _, sE, zE = oracle.prefill(ke[b:b + 1, :, pe:], ke[b:b + 1, :, pe:], ve[b:b + 1, :, pe:])
+        sD = np.zeros_like(sE); zD = np.zeros_like(zE)
+        if p < N:
+            _, sD, zD = oracle.prefill(q[b:b + 1, :, p:], k[b:b + 1, :, p:], v[b:b + 1, :, p:])
+        assert rel(s[b:b + 1], s0[b:b + 1] + sE + sD) < 1e-13
+        assert rel(z[b:b + 1], z0[b:b + 1] + zE + zD) < 1e-13
+    # a fully padded row keeps its initial state exactly
+    assert np.array_equal(s[2], s0[2]) and np.array_equal(z[2], z0[2])
+
+
+def test_zero_padding_is_no_padding_and_bad_pads_are_rejected():
+    """p_b = 0 everywhere is the unpadded call bit for bit; p_b outside
+    [0, N] is an error."""
+    M, N = 7, 11
+    q, k, v, ke, ve = _padded_case(M, N, [0, 0])
+    a = oracle.prefix_prefill(q, k, v, ke, ve, left_pad=[0, 0])
+    b = oracle.prefix_prefill(q, k, v, ke, ve)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    with pytest.raises(RuntimeError):
+        oracle.prefix_prefill(q, k, v, ke, ve, left_pad=[0, N + 1])
+    with pytest.raises(RuntimeError):
+        oracle.prefill(q, k, v, left_pad=[-1, 0])
