@@ -6,6 +6,8 @@ long-prefill workload (B=16, H=16, N=32768, bf16, non-zero s0/z0 from a
 each token covering all 16 heads), summed over ranks.  The same run also
 times the other two calls of the path, reported under ``legs``:
   - prefix: la_prefix_prefill on the JRT-RNN workload (N=32768, M=16384);
+  - prefix_padded: the same workload as a left-padded batch (per-row padding
+    counts uniform in [0, M], la_prefix_prefill_padded);
   - decode: la_decode_step on B=128, H=16, 512 consecutive steps captured in
     one CUDA graph, state from a 2048-token prefill (tokens/s and HBM GB/s).
 Inputs are seeded synthetic tensors already resident in HBM and larger than
@@ -311,6 +313,33 @@ def leg_prefix(la, args, dist, dev):
     return {"ms": ms, "B": B, "H": H, "N": N, "M": M}
 
 
+def leg_prefix_padded(la, args, dist, dev):
+    """The JRT-RNN prefix workload as a left-padded batch: row b's first p_b
+    positions are padding, p_b drawn uniformly in [0, M] (seeded)."""
+    w = inputs.WORKLOADS[4]
+    B, H, N, M = w.B, w.H, w.N, w.M
+    g = torch.Generator(device=dev)
+    g.manual_seed(shard_seed(w.seed + 17, dist.rank))
+    q = gen_device((B, H, N, 16), g, dev=dev)
+    k = gen_device((B, H, N, 16), g, dev=dev)
+    v = gen_device((B, H, N, 64), g, dev=dev)
+    ke = gen_device((B, H, M, 16), g, dev=dev)
+    ve = gen_device((B, H, M, 64), g, dev=dev)
+    pads = torch.randint(0, M + 1, (B,), generator=g, device=dev, dtype=torch.int32)
+    ws = torch.empty(la.prefix_workspace_size(B, H, M), dtype=torch.uint8, device=dev)
+    y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
+    s = torch.empty((B, H, 273, 64), dtype=torch.float32, device=dev)
+    z = torch.empty((B, H, 273), dtype=torch.float32, device=dev)
+
+    def step():
+        la.prefix_prefill(q, k, v, ke, ve, y=y, s_out=s, z_out=z, workspace=ws, left_pad=pads)
+
+    ms = time_loop(step, max(1, args.steps // 2), max(3, args.warmup // 2), dist)
+    la.check_device_status()
+    valid = int((N - pads.to(torch.int64)).sum().item())
+    return {"ms": ms, "B": B, "H": H, "N": N, "M": M, "valid_tokens": valid}
+
+
 def leg_decode(la, args, dist, dev):
     w = inputs.WORKLOADS[5]
     B, H, T = w.B, w.H, args.decode_steps
@@ -410,7 +439,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="prefill,prefix,decode")
+    ap.add_argument("--legs", default="prefill,prefix,prefix_padded,decode")
     ap.add_argument("--decode-steps", type=int, default=512)
     ap.add_argument("--cpu-sample-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -441,6 +470,8 @@ def main():
     res = {}
     if "prefix" in legs:
         res["prefix"] = leg_prefix(la, args, dist, dev)
+    if "prefix_padded" in legs:
+        res["prefix_padded"] = leg_prefix_padded(la, args, dist, dev)
     if "decode" in legs:
         res["decode"] = leg_decode(la, args, dist, dev)
     pre["clocks"] = clocks.stop()
@@ -500,6 +531,14 @@ def main():
             "tokens_per_s": W * r["B"] * r["N"] / t, "achieved_tflops": fl / t / 1e12,
             "tc_frac": fl / t / 1e12 / pk["bf16_tflops"], "hbm_gbs": by / t / 1e9,
             "hbm_frac": by / t / 1e9 / pk["hbm_gbs"]}
+        launches += 3 * max(1, args.steps // 2)
+    if "prefix_padded" in res:
+        r = res["prefix_padded"]
+        t = r["ms"] / 1e3
+        line["legs"]["prefix_padded"] = {
+            "workload": inputs.WORKLOADS[4].name + "-leftpad-uniform0toM", "ms_per_call": r["ms"],
+            "tokens_per_s": W * r["B"] * r["N"] / t,
+            "valid_tokens_per_s": W * r["valid_tokens"] / t}
         launches += 3 * max(1, args.steps // 2)
     if "decode" in res:
         r = res["decode"]

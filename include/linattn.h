@@ -135,6 +135,44 @@ LA_API la_status la_prefix_prefill(const void *q, const void *k, const void *v,
                             la_dtype dtype, float eps, la_stream_t stream);
 
 /*
+ * la_prefill_padded, la_prefix_prefill_padded -- the same two calls for a
+ * batch of left-padded sequences ("Just read twice" reading notes, sec. 2.7:
+ * prompts shorter than M are left-padded to M and the padding is masked in
+ * the prefix linear attention; sec. 4.7: padding must stay out of the
+ * linear-attention state).
+ *
+ *   left_pad  in  [B] int32, DEVICE pointer, 4-byte aligned, required:
+ *             row b's first p_b = left_pad[b] positions are padding,
+ *             0 <= p_b <= N.
+ *
+ * For row b, prefix positions j < min(p_b, M) and causal positions i < p_b
+ * contribute nothing to s_E, the causal sums or the final state, and
+ * y_i = 0 for i < p_b.  Every other output equals that of the unpadded call
+ * on the valid tokens alone (q, k, v from position p_b on, k_e, v_e from
+ * min(p_b, M) on).  p_b = 0 for every row gives the unpadded result.
+ *
+ * The counts live in device memory and are checked there: a count outside
+ * [0, N] is clamped to that range and recorded in the device status word, so
+ * the next la_check_device_status returns LA_ERR_INVALID_ARG.  A NULL
+ * left_pad is LA_ERR_INVALID_ARG; left_pad must not overlap an output.
+ * All other arguments, layouts and errors are those of la_prefill /
+ * la_prefix_prefill.
+ */
+LA_API la_status la_prefill_padded(const void *q, const void *k, const void *v,
+                                   const float *s0, const float *z0, const int32_t *left_pad,
+                                   void *y, float *s_out, float *z_out,
+                                   int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                                   la_dtype dtype, float eps, la_stream_t stream);
+
+LA_API la_status la_prefix_prefill_padded(const void *q, const void *k, const void *v,
+                                          const void *k_e, const void *v_e, int64_t M,
+                                          const float *s0, const float *z0, const int32_t *left_pad,
+                                          void *y, float *s_out, float *z_out,
+                                          void *workspace, size_t workspace_bytes,
+                                          int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                                          la_dtype dtype, float eps, la_stream_t stream);
+
+/*
  * la_decode_step -- one recurrent decode step per (b, h) (BASED reading
  * notes, sec. 2.2 Eq. (2) for one token; sec. 2.5 notes that decoding still
  * reads and writes the whole persistent state).  The state is updated first
@@ -195,7 +233,9 @@ LA_API const char *la_status_string(la_status status);
  * la_check_device_status -- synchronizes `stream`, then reads and clears the
  * library's device status word on the current device.  Returns LA_ERR_TIMEOUT
  * if any kernel since the last check gave up a bounded wait (its outputs are
- * then undefined), LA_ERR_CUDA if the synchronization failed, LA_OK else.
+ * then undefined), else LA_ERR_INVALID_ARG if a padded call met a padding
+ * count outside [0, N] (it was clamped), LA_ERR_CUDA if the synchronization
+ * failed, LA_OK else.
  */
 LA_API la_status la_check_device_status(la_stream_t stream);
 

@@ -38,9 +38,13 @@ _VP, _FP, _I64, _I, _F, _SZ = (ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
 SIGNATURES = {
     "la_prefill": (_I, [_VP, _VP, _VP, _FP, _FP, _VP, _FP, _FP, _I64, _I64, _I64, _I, _I,
                         _I, _F, _VP]),
+    "la_prefill_padded": (_I, [_VP, _VP, _VP, _FP, _FP, _VP, _VP, _FP, _FP, _I64, _I64, _I64, _I,
+                               _I, _I, _F, _VP]),
     "la_prefix_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "la_prefix_prefill": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _FP, _FP, _VP,
                                _SZ, _I64, _I64, _I64, _I, _I, _I, _F, _VP]),
+    "la_prefix_prefill_padded": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _VP, _FP, _FP,
+                                      _VP, _SZ, _I64, _I64, _I64, _I, _I, _I, _F, _VP]),
     "la_decode_step": (_I, [_VP, _VP, _VP, _FP, _FP, _FP, _FP, _VP, _I64, _I64, _I, _I, _I,
                             _F, _VP]),
     "la_prefix_prefill_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _FP, _FP,
@@ -111,10 +115,17 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _need_pad(left_pad, B):
+    if left_pad is not None:
+        _need(left_pad, "left_pad", (B,), torch.int32)
+
+
 def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
-            z_out=None, want_state: bool = True, stream=None):
+            z_out=None, want_state: bool = True, stream=None, left_pad=None):
     """Causal prefill (la_prefill).  q,k [B,H,N,16], v [B,H,N,64] (bf16 or fp32,
     CUDA, contiguous); s0 [B,H,273,64], z0 [B,H,273] fp32 or None.
+    left_pad: CUDA int32 [B] counts of leading padding positions per batch row
+    (la_prefill_padded), or None.
     Returns (y, s_out, z_out); the states are None when want_state is False."""
     lib = load_library()
     B, H, N, _ = q.shape
@@ -137,8 +148,14 @@ def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
         _need(s_out, "s_out", (B, H, D_PHI, D_V), torch.float32)
     if z_out is not None:
         _need(z_out, "z_out", (B, H, D_PHI), torch.float32)
-    _raise(lib.la_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
-                          _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q), float(eps), _stream(stream)))
+    _need_pad(left_pad, B)
+    if left_pad is None:
+        _raise(lib.la_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
+                              _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q), float(eps), _stream(stream)))
+    else:
+        _raise(lib.la_prefill_padded(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(left_pad),
+                                     _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q),
+                                     float(eps), _stream(stream)))
     return y, s_out, z_out
 
 
@@ -148,10 +165,12 @@ def prefix_workspace_size(B: int, H: int, M: int) -> int:
 
 def prefix_prefill(q, k, v, k_e, v_e, s0=None, z0=None, *, eps: float = 0.0, y=None,
                    s_out=None, z_out=None, want_state: bool = True, workspace=None,
-                   stream=None):
+                   stream=None, left_pad=None):
     """JRT-RNN prefix linear attention (la_prefix_prefill).  k_e [B,H,M,16],
     v_e [B,H,M,64] with M <= N.  ``workspace`` is a CUDA uint8 tensor of at
-    least prefix_workspace_size(B, H, M) bytes (allocated here if None)."""
+    least prefix_workspace_size(B, H, M) bytes (allocated here if None).
+    left_pad: CUDA int32 [B] counts of leading padding positions per batch row
+    (la_prefix_prefill_padded), or None."""
     lib = load_library()
     B, H, N, _ = q.shape
     dt = q.dtype
@@ -174,10 +193,17 @@ def prefix_prefill(q, k, v, k_e, v_e, s0=None, z0=None, *, eps: float = 0.0, y=N
     need = prefix_workspace_size(B, H, M)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    _raise(lib.la_prefix_prefill(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(k_e), _ptr(v_e), M, _ptr(s0), _ptr(z0), _ptr(y),
-        _ptr(s_out), _ptr(z_out), _ptr(workspace), workspace.numel(), B, H, N, D_FEAT, D_V,
-        _dt(q), float(eps), _stream(stream)))
+    _need_pad(left_pad, B)
+    if left_pad is None:
+        _raise(lib.la_prefix_prefill(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(k_e), _ptr(v_e), M, _ptr(s0), _ptr(z0), _ptr(y),
+            _ptr(s_out), _ptr(z_out), _ptr(workspace), workspace.numel(), B, H, N, D_FEAT, D_V,
+            _dt(q), float(eps), _stream(stream)))
+    else:
+        _raise(lib.la_prefix_prefill_padded(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(k_e), _ptr(v_e), M, _ptr(s0), _ptr(z0), _ptr(left_pad),
+            _ptr(y), _ptr(s_out), _ptr(z_out), _ptr(workspace), workspace.numel(), B, H, N, D_FEAT,
+            D_V, _dt(q), float(eps), _stream(stream)))
     return y, s_out, z_out
 
 

@@ -131,10 +131,16 @@ const char *la_status_string(la_status s) {
     return "unknown status";
 }
 
-la_status la_prefill(const void *q, const void *k, const void *v, const float *s0,
-                     const float *z0, void *y, float *s_out, float *z_out, int64_t B,
-                     int64_t H, int64_t N, int d_feat, int d_v, la_dtype dtype, float eps,
-                     la_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+la_status prefill_impl(const void *q, const void *k, const void *v, const float *s0,
+                       const float *z0, const int32_t *left_pad, void *y, float *s_out,
+                       float *z_out, int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                       la_dtype dtype, float eps, la_stream_t stream) {
     la_status st = check_common(B, H, N, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
     if ((s0 == nullptr) != (z0 == nullptr)) return LA_ERR_INVALID_ARG;
@@ -150,30 +156,29 @@ la_status la_prefill(const void *q, const void *k, const void *v, const float *s
     const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * kD * kDV},
                          {z_out, sizeof(float) * BH * kD}};
     if (any_overlap(in, 5, out, 3)) return LA_ERR_INVALID_ARG;
+    if (left_pad && !aligned4(left_pad)) return LA_ERR_MISALIGNED;
+    if (overlaps({left_pad, sizeof(int32_t) * B}, out[0]) || overlaps({left_pad, sizeof(int32_t) * B}, out[1]) ||
+        overlaps({left_pad, sizeof(int32_t) * B}, out[2]))
+        return LA_ERR_INVALID_ARG;
     int dev;
     unsigned *status;
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
-    la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status};
+    la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad};
     return to_status(run_prefill(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-size_t la_prefix_workspace_size(int64_t B, int64_t H, int64_t M) {
-    if (B < 1 || H < 1 || M <= 0 || B > kMaxBH / H) return 0;
-    return prefix_layout(B * H, M).total;
-}
-
-la_status la_prefix_prefill(const void *q, const void *k, const void *v, const void *k_e,
-                            const void *v_e, int64_t M, const float *s0, const float *z0,
-                            void *y, float *s_out, float *z_out, void *workspace,
-                            size_t workspace_bytes, int64_t B, int64_t H, int64_t N,
-                            int d_feat, int d_v, la_dtype dtype, float eps,
-                            la_stream_t stream) {
+la_status prefix_impl(const void *q, const void *k, const void *v, const void *k_e,
+                      const void *v_e, int64_t M, const float *s0, const float *z0,
+                      const int32_t *left_pad, void *y, float *s_out, float *z_out,
+                      void *workspace, size_t workspace_bytes, int64_t B, int64_t H,
+                      int64_t N, int d_feat, int d_v, la_dtype dtype, float eps,
+                      la_stream_t stream) {
     la_status st = check_common(B, H, N, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
     if (M < 0 || M > N) return LA_ERR_INVALID_ARG;
     if (M == 0)
-        return la_prefill(q, k, v, s0, z0, y, s_out, z_out, B, H, N, d_feat, d_v, dtype,
-                          eps, stream);
+        return prefill_impl(q, k, v, s0, z0, left_pad, y, s_out, z_out, B, H, N, d_feat, d_v,
+                            dtype, eps, stream);
     if ((s0 == nullptr) != (z0 == nullptr)) return LA_ERR_INVALID_ARG;
     if (!q || !k || !v || !y || !k_e || !v_e || !workspace) return LA_ERR_INVALID_ARG;
     const int64_t BH = B * H;
@@ -191,6 +196,12 @@ la_status la_prefix_prefill(const void *q, const void *k, const void *v, const v
     const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * kD * kDV},
                          {z_out, sizeof(float) * BH * kD}, {workspace, L.total}};
     if (any_overlap(in, 7, out, 4)) return LA_ERR_INVALID_ARG;
+    if (left_pad) {
+        if (!aligned4(left_pad)) return LA_ERR_MISALIGNED;
+        const Range lp{left_pad, sizeof(int32_t) * B};
+        for (const Range &o : out)
+            if (overlaps(lp, o)) return LA_ERR_INVALID_ARG;
+    }
     int dev;
     unsigned *status;
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
@@ -205,13 +216,62 @@ la_status la_prefix_prefill(const void *q, const void *k, const void *v, const v
     pa.s_init = reinterpret_cast<float *>(ws + L.s_init);
     pa.z_init = reinterpret_cast<float *>(ws + L.z_init);
     pa.status = status;
+    pa.left_pad = left_pad;
+    pa.N = N;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = dtype == LA_DTYPE_BF16 ? la::launch_prefix_partials_tc(pa, cs)
                                            : la::launch_prefix_partials_simt(pa, dtype, cs);
     if (e == cudaSuccess) e = la::launch_prefix_reduce(pa, cs);
     if (e != cudaSuccess) return LA_ERR_CUDA;
-    la::PrefillArgs a{q, k, v, pa.s_init, pa.z_init, y, s_out, z_out, B, H, N, eps, status};
+    la::PrefillArgs a{q, k, v, pa.s_init, pa.z_init, y, s_out, z_out, B, H, N, eps, status, left_pad};
     return to_status(run_prefill(a, dtype, cs));
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status la_prefill(const void *q, const void *k, const void *v, const float *s0,
+                     const float *z0, void *y, float *s_out, float *z_out, int64_t B,
+                     int64_t H, int64_t N, int d_feat, int d_v, la_dtype dtype, float eps,
+                     la_stream_t stream) {
+    return prefill_impl(q, k, v, s0, z0, nullptr, y, s_out, z_out, B, H, N, d_feat, d_v, dtype,
+                        eps, stream);
+}
+
+la_status la_prefill_padded(const void *q, const void *k, const void *v, const float *s0,
+                            const float *z0, const int32_t *left_pad, void *y, float *s_out,
+                            float *z_out, int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                            la_dtype dtype, float eps, la_stream_t stream) {
+    if (!left_pad) return LA_ERR_INVALID_ARG;
+    return prefill_impl(q, k, v, s0, z0, left_pad, y, s_out, z_out, B, H, N, d_feat, d_v, dtype,
+                        eps, stream);
+}
+
+size_t la_prefix_workspace_size(int64_t B, int64_t H, int64_t M) {
+    if (B < 1 || H < 1 || M <= 0 || B > kMaxBH / H) return 0;
+    return prefix_layout(B * H, M).total;
+}
+
+la_status la_prefix_prefill(const void *q, const void *k, const void *v, const void *k_e,
+                            const void *v_e, int64_t M, const float *s0, const float *z0,
+                            void *y, float *s_out, float *z_out, void *workspace,
+                            size_t workspace_bytes, int64_t B, int64_t H, int64_t N,
+                            int d_feat, int d_v, la_dtype dtype, float eps,
+                            la_stream_t stream) {
+    return prefix_impl(q, k, v, k_e, v_e, M, s0, z0, nullptr, y, s_out, z_out, workspace,
+                       workspace_bytes, B, H, N, d_feat, d_v, dtype, eps, stream);
+}
+
+la_status la_prefix_prefill_padded(const void *q, const void *k, const void *v, const void *k_e,
+                                   const void *v_e, int64_t M, const float *s0, const float *z0,
+                                   const int32_t *left_pad, void *y, float *s_out, float *z_out,
+                                   void *workspace, size_t workspace_bytes, int64_t B, int64_t H,
+                                   int64_t N, int d_feat, int d_v, la_dtype dtype, float eps,
+                                   la_stream_t stream) {
+    if (!left_pad) return LA_ERR_INVALID_ARG;
+    return prefix_impl(q, k, v, k_e, v_e, M, s0, z0, left_pad, y, s_out, z_out, workspace,
+                       workspace_bytes, B, H, N, d_feat, d_v, dtype, eps, stream);
 }
 
 la_status la_decode_step(const void *q, const void *k, const void *v, const float *s_in,
@@ -257,7 +317,7 @@ la_status la_check_device_status(la_stream_t stream) {
         const unsigned zero = 0;
         if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return LA_ERR_CUDA;
-        return LA_ERR_TIMEOUT;
+        return (word & la::kStatusTimeout) ? LA_ERR_TIMEOUT : LA_ERR_INVALID_ARG;
     }
     return LA_OK;
 }

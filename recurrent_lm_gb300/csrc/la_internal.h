@@ -17,6 +17,20 @@ constexpr int kStateFloats = kD * kDV + kD;  // one head's s and z
 
 // Bits of the device status word (one per failure class).
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusBadPad = 2u;   // a left-padding count outside [0, N] (clamped)
+
+// Leading padding positions of batch row b: left_pad[b] clamped to [0, N]
+// (NULL: none).  An out-of-range count sets kStatusBadPad (by one thread).
+__device__ __forceinline__ int64_t row_left_pad(const int32_t *left_pad, int64_t b, int64_t N,
+                                                unsigned *status, bool report) {
+    if (!left_pad) return 0;
+    const int64_t p = left_pad[b];
+    if (p < 0 || p > N) {
+        if (report) atomicOr(status, kStatusBadPad);
+        return p < 0 ? 0 : N;
+    }
+    return p;
+}
 
 struct PrefillArgs {
     const void *q, *k, *v;
@@ -26,6 +40,7 @@ struct PrefillArgs {
     int64_t B, H, N;
     float eps;
     unsigned *status;   // device status word
+    const int32_t *left_pad;  // [B] leading padding positions per batch row, or NULL
 };
 
 struct DecodeArgs {
@@ -47,6 +62,8 @@ struct PrefixArgs {
     const float *s0, *z0;
     float *s_init, *z_init;   // s0 + s_E, z0 + z_E  [BH][273][64], [BH][273]
     unsigned *status;
+    const int32_t *left_pad;  // [B]: prefix positions j < min(left_pad[b], M) are padding
+    int64_t N;                // causal length (the range of left_pad)
 };
 
 // Token-segment length of the prefix reduction and its workspace layout.

@@ -41,7 +41,8 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const T *__restrict__ v, const float *__restrict__ s0,
                     const float *__restrict__ z0, T *__restrict__ y,
                     float *__restrict__ s_out, float *__restrict__ z_out,
-                    int64_t N, float eps) {
+                    int64_t N, float eps, const int32_t *__restrict__ left_pad, int64_t H,
+                    unsigned *status) {
     __shared__ float xq[kDFeat], xk[kDFeat], vs[kDV];
     __shared__ float phq[kD], phk[kD];
     __shared__ float zsh[kD];
@@ -60,7 +61,11 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
     }
     for (int f = tid; f < kD; f += kThreads) zsh[f] = z0 ? z0[bh * kD + f] : 0.f;
 
-    for (int64_t i = 0; i < N; ++i) {
+    // leading padding positions of this batch row: y = 0, no state change
+    const int64_t lpad = row_left_pad(left_pad, bh / H, N, status, tid == 0);
+    for (int64_t i = 0; i < lpad; ++i)
+        if (tid < kDV) Act<T>::store(y, (bh * N + i) * kDV + tid, 0.f);
+    for (int64_t i = lpad; i < N; ++i) {
         const int64_t t = bh * N + i;
         load_token(q, k, v, t * kDFeat, t * kDV, xq, xk, vs, tid);
         __syncthreads();
@@ -119,15 +124,18 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
 prefix_partial_simt_kernel(const T *__restrict__ ke, const T *__restrict__ ve,
                            int64_t M, int64_t seg_len, int64_t nseg,
-                           float *__restrict__ part_s, float *__restrict__ part_z) {
+                           float *__restrict__ part_s, float *__restrict__ part_z,
+                           const int32_t *__restrict__ left_pad, int64_t H, int64_t N) {
     __shared__ float xk[kDFeat], vs[kDV];
     __shared__ float phk[kD];
     __shared__ float zsh[kD];
     const int64_t bh = blockIdx.x, seg = blockIdx.y;
     const int tid = threadIdx.x;
     const int c = tid % kDV, g = tid / kDV;
-    const int64_t j0 = seg * seg_len;
-    const int64_t j1 = (j0 + seg_len < M) ? j0 + seg_len : M;
+    const int64_t j1 = (seg * seg_len + seg_len < M) ? seg * seg_len + seg_len : M;
+    // prefix positions below min(left pad, M) are padding (range reported by the prefill)
+    const int64_t pe = min(M, row_left_pad(left_pad, bh / H, N, nullptr, false));
+    const int64_t j0 = max(seg * seg_len, pe);
 
     float s[kRowsPerThread];
 #pragma unroll
@@ -218,11 +226,11 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, la_dtype dt, cudaStream_t 
         prefill_simt_kernel<__nv_bfloat16><<<(unsigned)BH, kThreads, 0, st>>>(
             (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k,
             (const __nv_bfloat16 *)a.v, a.s0, a.z0, (__nv_bfloat16 *)a.y, a.s_out,
-            a.z_out, a.N, a.eps);
+            a.z_out, a.N, a.eps, a.left_pad, a.H, a.status);
     else
         prefill_simt_kernel<float><<<(unsigned)BH, kThreads, 0, st>>>(
             (const float *)a.q, (const float *)a.k, (const float *)a.v, a.s0, a.z0,
-            (float *)a.y, a.s_out, a.z_out, a.N, a.eps);
+            (float *)a.y, a.s_out, a.z_out, a.N, a.eps, a.left_pad, a.H, a.status);
     return cudaGetLastError();
 }
 
@@ -232,11 +240,11 @@ cudaError_t launch_prefix_partials_simt(const PrefixArgs &a, la_dtype dt, cudaSt
     if (dt == LA_DTYPE_BF16)
         prefix_partial_simt_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(
             (const __nv_bfloat16 *)a.k_e, (const __nv_bfloat16 *)a.v_e, a.M,
-            a.seg_len, a.nseg, a.part_s, a.part_z);
+            a.seg_len, a.nseg, a.part_s, a.part_z, a.left_pad, a.H, a.N);
     else
         prefix_partial_simt_kernel<float><<<grid, kThreads, 0, st>>>(
             (const float *)a.k_e, (const float *)a.v_e, a.M, a.seg_len, a.nseg,
-            a.part_s, a.part_z);
+            a.part_s, a.part_z, a.left_pad, a.H, a.N);
     return cudaGetLastError();
 }
 

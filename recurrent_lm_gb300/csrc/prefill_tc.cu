@@ -144,11 +144,14 @@ __device__ uint32_t g_trace[5][kTraceChunks][8];
 #endif
 enum { TR_TMA = 0, TR_MMA, TR_GEN, TR_EPI, TR_CONV };
 
+// kPad: the launch carries per-row left-padding counts (a separate
+// instantiation, so the unpadded kernel carries none of the masking code).
+template <bool kPad>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty,
                   const float *__restrict__ s0,
-                  const float *__restrict__ z0, __nv_bfloat16 *__restrict__ y,
+                  const float *__restrict__ z0, const int32_t *__restrict__ left_pad, int64_t H,
                   float *__restrict__ s_out, float *__restrict__ z_out, int N, float eps,
                   unsigned *status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -165,6 +168,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const long long t_start = clock64();
 #endif
     const int n = (N + kC - 1) / kC;
+    // leading padding positions of this batch row: no contribution to any sum, y = 0
+    const int lpad = kPad ? (int)row_left_pad(left_pad, bh / H, N, status, tid == 0) : 0;
     // per-head columns of the ABI state: entry (row r, value d) at [r * 64 + d]
     const float *s0h = s0 ? s0 + bh * (int64_t)kD * kDV : nullptr;
     const float *z0h = z0 ? z0 + bh * (int64_t)kD : nullptr;
@@ -381,7 +386,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PHQ_FULL));
             if (tid == 128) LA_TR(TR_GEN, c, 1);
-            const bool pad = c * kC + t >= N;  // past the end: no contribution to S', z'
+            // past the end or left padding: no contribution to S', z'
+            bool pad = c * kC + t >= N;
+            if constexpr (kPad) pad = pad || c * kC + t < lpad;
             // the update of chunk c - 1 (S_FULL) released the Phi'_K buffer and V(c - 1)
             if (!mbar_wait(bar(B_S_FULL), pc ^ 1u, abort, status)) break;
             if (c > 0 && tid == 128) mbar_arrive(bar(B_V_EMPTY + (c - 1) % kStages));
@@ -406,6 +413,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             __syncwarp();  // tcgen05.ld/st below are warp-collective (.sync.aligned)
             tc_fence_after();
             const uint32_t tb = tmem + lanebase + tm_t(b);
+            const int kmin = kPad ? lpad - c * kC : 0;  // keys below kmin are left padding
             // keys 64 pp .. 64 pp + 63 -> packed columns 32 pp .. 32 pp + 31, written only
             // after the T columns they overwrite have been read; rows of warp w only see
             // keys < 32 (w + 1)
@@ -429,6 +437,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                             if (key + 1 > i) p1 = 0.f;
                         }
                         pw[j] = pack_bf16(p0, p1);
+                    }
+                    if (kPad && kmin > 64 * pp) {  // chunk holds left padding: drop padded keys
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int key = 64 * pp + 2 * j;
+                            if (key + 1 < kmin) pw[j] = 0u;
+                            else if (key < kmin) pw[j] &= 0xFFFF0000u;  // low half = the even key
+                        }
                     }
                 } else {
 #pragma unroll
@@ -486,7 +502,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (lane == 0) mbar_arrive(bar(B_NUM_EMPTY));
                 // y rows of this warp -> its 4 KB staging tile -> one bulk tensor store
                 // (rows past N are clipped by the store)
-                const float inv = 1.0f / (__uint_as_float(dr) + eps);
+                float inv = 1.0f / (__uint_as_float(dr) + eps);
+                if constexpr (kPad)
+                    if (c * kC + i < lpad) inv = 0.f;  // padded query rows (left padding) output 0
                 const uint64_t inv2 = f2pack(inv, inv);
                 const uint32_t stage = sb + kSmY + (uint32_t)w * 4096;
                 if (lane == 0) bulk_wait_read0();  // previous chunk's store has read the tile
@@ -601,13 +619,20 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
-    prefill_tc_kernel<<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-        tq, tk, tv, ty, a.s0, a.z0, (__nv_bfloat16 *)a.y, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+    if (a.left_pad)
+        prefill_tc_kernel<true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
+            tq, tk, tv, ty, a.s0, a.z0, a.left_pad, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+    else
+        prefill_tc_kernel<false><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
+            tq, tk, tv, ty, a.s0, a.z0, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
     return cudaGetLastError();
 }
 

@@ -46,7 +46,8 @@ constexpr uint32_t kIdUp = idesc_bf16(128, kNFeat, true, true);  // [V | 1]^T x 
 __global__ void __launch_bounds__(kThreads, 2)
 prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                          int M, int seg_len, int nseg, float *__restrict__ part_s,
-                         float *__restrict__ part_z, unsigned *status) {
+                         float *__restrict__ part_z, unsigned *status,
+                         const int32_t *__restrict__ left_pad, int64_t H, int64_t N) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -61,6 +62,8 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
     const int j0 = seg * seg_len;
     const int j1 = min(M, j0 + seg_len);
     const int n = (j1 - j0 + kC - 1) / kC;
+    // prefix positions below min(left pad, M) are padding (range reported by the prefill)
+    const int pe = (int)min((int64_t)M, row_left_pad(left_pad, bh / H, N, status, false));
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -140,7 +143,8 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_KV_EMPTY + st));
             if (!mbar_wait(bar(B_PHK_EMPTY), ((uint32_t)c & 1u) ^ 1u, abort, status)) break;
-            const bool pad = j0 + c * kC + t >= j1;  // outside this segment: no contribution
+            // outside this segment, or left padding: no contribution
+            const bool pad = j0 + c * kC + t >= j1 || j0 + c * kC + t < pe;
             emit_features<true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
             fence_async_smem();
             __syncwarp();
@@ -190,7 +194,8 @@ cudaError_t launch_prefix_partials_tc(const PrefixArgs &a, cudaStream_t st) {
     }
     dim3 grid((unsigned)BH, (unsigned)a.nseg);
     prefix_partial_tc_kernel<<<grid, kThreads, kSmAlloc, st>>>(tk, tv, (int)a.M, (int)a.seg_len,
-                                                               (int)a.nseg, a.part_s, a.part_z, a.status);
+                                                               (int)a.nseg, a.part_s, a.part_z, a.status,
+                                                               a.left_pad, a.H, a.N);
     return cudaGetLastError();
 }
 

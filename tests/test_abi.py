@@ -156,3 +156,24 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mod.load_library(str(tmp_path / "nope.so"))
     finally:
         mod._lib = saved
+
+
+def test_padded_calls_reject_null_misaligned_or_overlapping_pads(lib):
+    """la_prefill_padded / la_prefix_prefill_padded: the pad counts are a
+    required 4-byte aligned device array that no output may overlap."""
+    p = [fake(i) for i in range(8)]
+    q, k, v, s0, z0, y, so, zo = p
+    args = (1, 1, 8, 16, 64, 1, 0.0, None)
+    assert lib.la_prefill_padded(q, k, v, s0, z0, None, y, so, zo, *args) == binding.LA_ERR_INVALID_ARG
+    assert lib.la_prefill_padded(q, k, v, s0, z0, fake(9, misalign=2), y, so, zo,
+                                 *args) == binding.LA_ERR_MISALIGNED
+    inside_y = ctypes.c_void_p(y.value + 32)
+    assert lib.la_prefill_padded(q, k, v, s0, z0, inside_y, y, so, zo, *args) == binding.LA_ERR_INVALID_ARG
+    ke, ve, ws = fake(10), fake(11), fake(12)
+    pargs = (1, 1, 8, 16, 64, 1, 0.0, None)
+    assert lib.la_prefix_prefill_padded(q, k, v, ke, ve, 4, s0, z0, None, y, so, zo, ws, 1 << 30,
+                                        *pargs) == binding.LA_ERR_INVALID_ARG
+    assert lib.la_prefix_prefill_padded(q, k, v, ke, ve, 4, s0, z0, fake(9, misalign=1), y, so, zo, ws,
+                                        1 << 30, *pargs) == binding.LA_ERR_MISALIGNED
+    assert lib.la_prefix_prefill_padded(q, k, v, ke, ve, 9, s0, z0, fake(9), y, so, zo, ws, 1 << 30,
+                                        *pargs) == binding.LA_ERR_INVALID_ARG  # M > N
