@@ -8,6 +8,8 @@ times the other two calls of the path, reported under ``legs``:
   - prefix: la_prefix_prefill on the JRT-RNN workload (N=32768, M=16384);
   - prefix_padded: the same workload as a left-padded batch (per-row padding
     counts uniform in [0, M], la_prefix_prefill_padded);
+  - jrt_prompt: the JRT-Prompt alternative, la_prefill over the prompt read
+    twice (2N = 65536 tokens), timed against the prefix call;
   - decode: la_decode_step on B=128, H=16, 512 consecutive steps captured in
     one CUDA graph, state from a 2048-token prefill (tokens/s and HBM GB/s).
 Inputs are seeded synthetic tensors already resident in HBM and larger than
@@ -340,6 +342,29 @@ def leg_prefix_padded(la, args, dist, dev):
     return {"ms": ms, "B": B, "H": H, "N": N, "M": M, "valid_tokens": valid}
 
 
+def leg_jrt_prompt(la, args, dist, dev):
+    """JRT-Prompt: the prompt read twice by plain causal prefill, i.e.
+    la_prefill at 2N = 65536 tokens (B=16, H=16), the pages' comparison
+    point for the JRT-RNN prefix call on the same prompt."""
+    w = inputs.WORKLOADS[4]
+    B, H, N2 = w.B, w.H, 2 * w.N
+    g = torch.Generator(device=dev)
+    g.manual_seed(shard_seed(w.seed + 29, dist.rank))
+    q = gen_device((B, H, N2, 16), g, dev=dev)
+    k = gen_device((B, H, N2, 16), g, dev=dev)
+    v = gen_device((B, H, N2, 64), g, dev=dev)
+    y = torch.empty((B, H, N2, 64), dtype=torch.bfloat16, device=dev)
+    s = torch.empty((B, H, 273, 64), dtype=torch.float32, device=dev)
+    z = torch.empty((B, H, 273), dtype=torch.float32, device=dev)
+
+    def step():
+        la.prefill(q, k, v, y=y, s_out=s, z_out=z)
+
+    ms = time_loop(step, max(1, args.steps // 4), max(3, args.warmup // 2), dist)
+    la.check_device_status()
+    return {"ms": ms, "B": B, "H": H, "N": w.N, "N_read": N2}
+
+
 def leg_decode(la, args, dist, dev):
     w = inputs.WORKLOADS[5]
     B, H, T = w.B, w.H, args.decode_steps
@@ -439,7 +464,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="prefill,prefix,prefix_padded,decode")
+    ap.add_argument("--legs", default="prefill,prefix,prefix_padded,jrt_prompt,decode")
     ap.add_argument("--decode-steps", type=int, default=512)
     ap.add_argument("--cpu-sample-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -472,6 +497,8 @@ def main():
         res["prefix"] = leg_prefix(la, args, dist, dev)
     if "prefix_padded" in legs:
         res["prefix_padded"] = leg_prefix_padded(la, args, dist, dev)
+    if "jrt_prompt" in legs:
+        res["jrt_prompt"] = leg_jrt_prompt(la, args, dist, dev)
     if "decode" in legs:
         res["decode"] = leg_decode(la, args, dist, dev)
     pre["clocks"] = clocks.stop()
@@ -540,6 +567,17 @@ def main():
             "tokens_per_s": W * r["B"] * r["N"] / t,
             "valid_tokens_per_s": W * r["valid_tokens"] / t}
         launches += 3 * max(1, args.steps // 2)
+    if "jrt_prompt" in res:
+        r = res["jrt_prompt"]
+        t = r["ms"] / 1e3
+        fl = r["B"] * r["H"] * r["N_read"] * FLOPS_PER_HEAD_TOKEN
+        entry = {"workload": f"jrt-prompt-bf16-B{r['B']}-H{r['H']}-N{r['N']}-read-twice",
+                 "ms_per_call": r["ms"], "prompt_tokens_per_s": W * r["B"] * r["N"] / t,
+                 "achieved_tflops": fl / t / 1e12, "tc_frac": fl / t / 1e12 / pk["bf16_tflops"]}
+        if "prefix" in line["legs"]:
+            entry["time_vs_jrt_rnn_prefix"] = r["ms"] / line["legs"]["prefix"]["ms_per_call"]
+        line["legs"]["jrt_prompt"] = entry
+        launches += max(1, args.steps // 4)
     if "decode" in res:
         r = res["decode"]
         per_step_ms = r["ms_per_graph"] / r["steps_per_graph"]

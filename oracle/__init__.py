@@ -82,6 +82,10 @@ def _load():
         lib.oracle_prefix_prefill_padded.restype = I
         lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, P, P, L, L, L, L, D, I]
         lib.oracle_decode_step.restype = I
+        lib.oracle_prefill_decay.argtypes = [P, P, P, P, P, P, P, P, P, L, L, L, L, L, D, I]
+        lib.oracle_prefill_decay.restype = I
+        lib.oracle_decode_step_decay.argtypes = [P, P, P, P, P, P, P, P, P, L, L, L, L, D, I]
+        lib.oracle_decode_step_decay.restype = I
         lib.oracle_prefill_chunked.argtypes = [P, P, P, P, P, P, P, P, L, L, L, L,
                                                L, L, D, I]
         lib.oracle_prefill_chunked.restype = I
@@ -184,8 +188,25 @@ def prefill_chunked(q, k, v, C: int, s0=None, z0=None, eps=0.0, nthreads: int = 
     return y, s, z
 
 
-def decode_step(q, k, v, s_in, z_in, eps=0.0, nthreads: int = 0):
-    """One recurrent step; q,k [B,H,dk], v [B,H,dv]; returns (y, s, z)."""
+def prefill_decay(q, k, v, gamma, s0=None, z0=None, eps=0.0, nthreads: int = 0):
+    """Causal prefill with a fixed per-head decay gamma [H] in [0, 1];
+    returns (y, s, z) in float64."""
+    q, k, v, s0, z0 = _f64(q), _f64(k), _f64(v), _f64(s0), _f64(z0)
+    B, H, N, dk, dv = _shapes(q, v)
+    D = feature_dim(dk)
+    g = np.ascontiguousarray(np.asarray(gamma, dtype=np.float64).reshape(H))
+    y = np.empty((B, H, N, dv), dtype=np.float64)
+    s = np.empty((B, H, D, dv), dtype=np.float64)
+    z = np.empty((B, H, D), dtype=np.float64)
+    _check(_load().oracle_prefill_decay(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(g), _ptr(y), _ptr(s), _ptr(z),
+        B, H, N, dk, dv, float(eps), int(nthreads)))
+    return y, s, z
+
+
+def decode_step(q, k, v, s_in, z_in, eps=0.0, nthreads: int = 0, gamma=None):
+    """One recurrent step; q,k [B,H,dk], v [B,H,dv]; gamma [H] per-head decay
+    or None; returns (y, s, z)."""
     q, k, v, s_in, z_in = _f64(q), _f64(k), _f64(v), _f64(s_in), _f64(z_in)
     B, H, dk = q.shape
     dv = v.shape[-1]
@@ -193,7 +214,8 @@ def decode_step(q, k, v, s_in, z_in, eps=0.0, nthreads: int = 0):
     y = np.empty((B, H, dv), dtype=np.float64)
     s = np.empty((B, H, D, dv), dtype=np.float64)
     z = np.empty((B, H, D), dtype=np.float64)
-    _check(_load().oracle_decode_step(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(s_in), _ptr(z_in), _ptr(s), _ptr(z),
+    g = None if gamma is None else np.ascontiguousarray(np.asarray(gamma, dtype=np.float64).reshape(H))
+    _check(_load().oracle_decode_step_decay(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(s_in), _ptr(z_in), _ptr(s), _ptr(z),
         _ptr(y), B, H, dk, dv, float(eps), int(nthreads)))
     return y, s, z

@@ -29,6 +29,11 @@
  *  - "Understanding and Improving Length Generalization in Recurrent Models"
  *    (reading notes), sec. 2.5 "non-zero initial state", Eq. (4): with the
  *    identity transition the initial state simply adds to the running sum.
+ *  - same page, sec. 2.1, Eq. (1): the general recurrence h_t = A_t h_{t-1}
+ *    + B_t x_t.  The decayed variants below take A_t = gamma_h I, a fixed
+ *    per-head decay (BASED page, sec. 2.4: fixed per-head decay rates in some
+ *    of its runs): s_t = gamma s_{t-1} + phi(k_t) v_t^T, z likewise, so the
+ *    initial state reaches token t (0-based) as gamma^(t+1) s0 (sec. 2.5).
  *
  * Layouts (all dense, row-major, double):
  *   q, k   [B][H][N][dk]      v, y  [B][H][N][dv]
@@ -68,15 +73,20 @@ static double dot(const double *a, const double *b, long n) {
 /* One recurrent step on one head: s += phi(k) v^T, z += phi(k), then
  * y = phi(q)^T s / (phi(q)^T z + eps).  The state includes the current token
  * before it is read (BASED page, Eq. (2): y_i uses s_i, not s_{i-1}). */
-static void step(const double *q, const double *k, const double *v, double *s,
-                 double *z, double *y, long dk, long dv, double eps,
-                 double *phq, double *phk) {
+static void step_decay(const double *q, const double *k, const double *v, double *s,
+                       double *z, double *y, long dk, long dv, double eps,
+                       double *phq, double *phk, double gamma, int decay) {
     const long D = oracle_feature_dim(dk);
     oracle_phi(k, dk, phk);
     oracle_phi(q, dk, phq);
     for (long f = 0; f < D; ++f) {
-        for (long c = 0; c < dv; ++c) s[f * dv + c] += phk[f] * v[c];
-        z[f] += phk[f];
+        if (decay) {
+            for (long c = 0; c < dv; ++c) s[f * dv + c] = gamma * s[f * dv + c] + phk[f] * v[c];
+            z[f] = gamma * z[f] + phk[f];
+        } else {
+            for (long c = 0; c < dv; ++c) s[f * dv + c] += phk[f] * v[c];
+            z[f] += phk[f];
+        }
     }
     const double den = dot(phq, z, D) + eps;
     for (long c = 0; c < dv; ++c) {
@@ -84,6 +94,12 @@ static void step(const double *q, const double *k, const double *v, double *s,
         for (long f = 0; f < D; ++f) num += phq[f] * s[f * dv + c];
         y[c] = num / den;
     }
+}
+
+static void step(const double *q, const double *k, const double *v, double *s,
+                 double *z, double *y, long dk, long dv, double eps,
+                 double *phq, double *phk) {
+    step_decay(q, k, v, s, z, y, dk, dv, eps, phq, phk, 1.0, 0);
 }
 
 static void load_state(const double *s0, const double *z0, long bh, long D,
@@ -198,13 +214,55 @@ int oracle_prefill(const double *q, const double *k, const double *v,
                                  B, H, N, dk, dv, eps, nthreads);
 }
 
+/* Causal prefill with a fixed per-head decay gamma[h] (0 <= gamma <= 1):
+ *   s_i = gamma s_{i-1} + phi(k_i) v_i^T,  z_i = gamma z_{i-1} + phi(k_i),
+ *   y_i = phi(q_i)^T s_i / (phi(q_i)^T z_i + eps),  s_{-1} = s0, z_{-1} = z0
+ * (length-generalization page, Eq. (1) with A_t = gamma I; Eq. (4)). */
+int oracle_prefill_decay(const double *q, const double *k, const double *v,
+                         const double *s0, const double *z0, const double *gamma,
+                         double *y, double *s_out, double *z_out, long B, long H, long N,
+                         long dk, long dv, double eps, int nthreads) {
+    if (dk < 1 || dk > 256 || dv < 1 || B < 0 || H < 0 || N < 0 || !gamma) return 1;
+    for (long h = 0; h < H; ++h)
+        if (!(gamma[h] >= 0.0 && gamma[h] <= 1.0)) return 1;
+    const long D = oracle_feature_dim(dk);
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = malloc(sizeof(double) * D * dv);
+        double *z = malloc(sizeof(double) * D);
+        double *phq = malloc(sizeof(double) * D);
+        double *phk = malloc(sizeof(double) * D);
+        if (!s || !z || !phq || !phk) {
+#pragma omp atomic write
+            err = 2;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long bh = 0; bh < B * H; ++bh) {
+                load_state(s0, z0, bh, D, dv, s, z);
+                for (long i = 0; i < N; ++i) {
+                    const long t = bh * N + i;
+                    step_decay(q + t * dk, k + t * dk, v + t * dv, s, z, y + t * dv, dk, dv,
+                               eps, phq, phk, gamma[bh % H], 1);
+                }
+                store_state(s_out, z_out, bh, D, dv, s, z);
+            }
+        }
+        free(s); free(z); free(phq); free(phk);
+    }
+    return err;
+}
+
 /* One decode step per (b, h): the same recurrence for a single token.
  * q, k [B][H][dk], v, y [B][H][dv]; s_out may equal s_in (in place). */
-int oracle_decode_step(const double *q, const double *k, const double *v,
-                       const double *s_in, const double *z_in, double *s_out,
-                       double *z_out, double *y, long B, long H, long dk,
-                       long dv, double eps, int nthreads) {
+int oracle_decode_step_decay(const double *q, const double *k, const double *v,
+                             const double *gamma, const double *s_in, const double *z_in,
+                             double *s_out, double *z_out, double *y, long B, long H,
+                             long dk, long dv, double eps, int nthreads) {
     if (dk < 1 || dk > 256 || dv < 1 || B < 0 || H < 0) return 1;
+    for (long h = 0; gamma && h < H; ++h)
+        if (!(gamma[h] >= 0.0 && gamma[h] <= 1.0)) return 1;
     const long D = oracle_feature_dim(dk);
     set_threads(nthreads);
     int err = 0;
@@ -221,14 +279,22 @@ int oracle_decode_step(const double *q, const double *k, const double *v,
 #pragma omp for schedule(static)
             for (long bh = 0; bh < B * H; ++bh) {
                 load_state(s_in, z_in, bh, D, dv, s, z);
-                step(q + bh * dk, k + bh * dk, v + bh * dv, s, z, y + bh * dv, dk,
-                     dv, eps, phq, phk);
+                step_decay(q + bh * dk, k + bh * dk, v + bh * dv, s, z, y + bh * dv, dk,
+                           dv, eps, phq, phk, gamma ? gamma[bh % H] : 1.0, gamma != NULL);
                 store_state(s_out, z_out, bh, D, dv, s, z);
             }
         }
         free(s); free(z); free(phq); free(phk);
     }
     return err;
+}
+
+int oracle_decode_step(const double *q, const double *k, const double *v,
+                       const double *s_in, const double *z_in, double *s_out,
+                       double *z_out, double *y, long B, long H, long dk,
+                       long dv, double eps, int nthreads) {
+    return oracle_decode_step_decay(q, k, v, NULL, s_in, z_in, s_out, z_out, y, B, H, dk, dv,
+                                    eps, nthreads);
 }
 
 /* The blockwise form of the same prefill (BASED page, sec. 2.5):

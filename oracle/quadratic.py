@@ -60,3 +60,40 @@ def prefix_closed_form(q, k, v, ke=None, ve=None, init_num=None, init_den=None,
 def prefill_closed_form(q, k, v, init_num=None, init_den=None, eps=0.0):
     """Causal closed form (BASED page, sec. 2.2, Eq. (1))."""
     return prefix_closed_form(q, k, v, None, None, init_num, init_den, eps)
+
+
+def prefill_decay_closed_form(q, k, v, gamma, s0=None, z0=None, eps=0.0):
+    """Causal form with a fixed per-head decay, written as sums over tokens
+    (length-generalization page, sec. 2.5, Eq. (4) with A_t = gamma I): for
+    0-based positions i, j
+      y_i = [gamma^(i+1) phi(q_i)^T s0 + sum_{j<=i} gamma^(i-j) K(q_i,k_j) v_j]
+          / [gamma^(i+1) phi(q_i)^T z0 + sum_{j<=i} gamma^(i-j) K(q_i,k_j) + eps].
+    gamma has shape [H]; phi(q)^T s0 uses the explicit feature map _phi_np."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, N, dk = q.shape
+    g = np.asarray(gamma, dtype=np.float64).reshape(1, H, 1, 1)
+    idx = np.arange(N)
+    diff = (idx[:, None] - idx[None, :]).astype(np.float64)
+    mask = (diff >= 0).astype(np.float64)
+    decay = np.where(diff[None, None] >= 0, g ** np.maximum(diff, 0)[None, None], 0.0)
+    A = _gram_kernel(q, k) * decay * mask[None, None]
+    num = np.einsum("bhij,bhjc->bhic", A, v)
+    den = A.sum(axis=-1)
+    if s0 is not None:
+        lam = g[..., 0] ** (idx + 1.0)[None, None]          # [1,H,N]
+        phq = _phi_np(q)                                   # [B,H,N,D]
+        num = num + lam[..., None] * np.einsum("bhid,bhdc->bhic", phq, np.asarray(s0, np.float64))
+        den = den + lam * np.einsum("bhid,bhd->bhi", phq, np.asarray(z0, np.float64))
+    return num / (den + eps)[..., None]
+
+
+def _phi_np(x):
+    """phi(x) = [1, xbar, vec(xbar xbar^T)/sqrt(2)], xbar = x / d'^(1/4), over
+    the last axis (BASED page, sec. 2.3), written out with numpy."""
+    x = np.asarray(x, dtype=np.float64)
+    dk = x.shape[-1]
+    xb = x / dk ** 0.25
+    quad = (xb[..., :, None] * xb[..., None, :]).reshape(*x.shape[:-1], dk * dk) / np.sqrt(2.0)
+    return np.concatenate([np.ones(x.shape[:-1] + (1,)), xb, quad], axis=-1)

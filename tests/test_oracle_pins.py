@@ -349,3 +349,72 @@ def test_zero_padding_is_no_padding_and_bad_pads_are_rejected():
         oracle.prefix_prefill(q, k, v, ke, ve, left_pad=[0, N + 1])
     with pytest.raises(RuntimeError):
         oracle.prefill(q, k, v, left_pad=[-1, 0])
+
+
+# ---------------------------------------------------------------- per-head decay
+def test_decay_one_is_no_decay_and_zero_keeps_only_the_current_token():
+    """LENGEN sec. 2.1 Eq. (1) with A_t = gamma I.  gamma = 1 is the plain
+    recurrence (bit for bit); gamma = 0 keeps only the current token, so
+    y_i = K(q_i,k_i) v_i / K(q_i,k_i) = v_i and the final state is
+    phi(k_N) v_N^T."""
+    N = 23
+    q = rnd(1, 2, N, 16); k = rnd(1, 2, N, 16); v = rnd(1, 2, N, 8)
+    s0 = rnd(1, 2, 273, 8); z0 = np.abs(rnd(1, 2, 273)) + 1.0
+    a = oracle.prefill_decay(q, k, v, [1.0, 1.0], s0, z0)
+    b = oracle.prefill(q, k, v, s0, z0)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    y, s, z = oracle.prefill_decay(q, k, v, [0.0, 0.0], s0, z0)
+    assert rel(y, v) < 1e-13
+    ph = np.stack([oracle.phi(k[0, h, -1]) for h in range(2)])
+    assert rel(s[0], ph[:, :, None] * v[0, :, -1][:, None, :]) < 1e-15
+    assert rel(z[0], ph) < 1e-15
+
+
+def test_decay_against_closed_form():
+    """LENGEN sec. 2.5 Eq. (4) with A_t = gamma I: token j reaches position i
+    with weight gamma^(i-j) and the initial state with gamma^(i+1); checked
+    against the decayed kernel closed form, per-head gammas."""
+    N = 37
+    q = rnd(2, 3, N, 16); k = rnd(2, 3, N, 16); v = rnd(2, 3, N, 8)
+    s0 = rnd(2, 3, 273, 8) * 0.1; z0 = np.abs(rnd(2, 3, 273)) + 2.0
+    gam = [0.5, 0.9, 0.999]
+    y, _, _ = oracle.prefill_decay(q, k, v, gam, s0, z0)
+    y_ref = quadratic.prefill_decay_closed_form(q, k, v, gam, s0, z0)
+    assert rel(y, y_ref) < 1e-12
+
+
+def test_decay_running_mean_when_kernel_is_one():
+    """q = 0 makes every kernel value 1, so y_i is the exponentially weighted
+    mean sum_j gamma^(i-j) v_j / sum_j gamma^(i-j) (a closed form)."""
+    N, gam = 40, 0.8
+    q = np.zeros((1, 1, N, 16)); k = rnd(1, 1, N, 16); v = rnd(1, 1, N, 4)
+    y, _, _ = oracle.prefill_decay(q, k, v, [gam])
+    for i in range(N):
+        w = gam ** (i - np.arange(i + 1))
+        assert rel(y[0, 0, i], (w[:, None] * v[0, 0, :i + 1]).sum(0) / w.sum()) < 1e-13
+
+
+def test_decay_state_passing_and_decode():
+    """The decayed recurrence splits at any point (LENGEN sec. 2.5): run(N1)
+    then run(N2) from its state equals run(N1+N2), and n decode steps equal
+    the prefill of those n tokens."""
+    N1, N2, gam = 11, 9, [0.93, 0.6]
+    q = rnd(1, 2, N1 + N2, 16); k = rnd(1, 2, N1 + N2, 16); v = rnd(1, 2, N1 + N2, 8)
+    y, s, z = oracle.prefill_decay(q, k, v, gam)
+    _, s1, z1 = oracle.prefill_decay(q[:, :, :N1], k[:, :, :N1], v[:, :, :N1], gam)
+    y2, s2, z2 = oracle.prefill_decay(q[:, :, N1:], k[:, :, N1:], v[:, :, N1:], gam, s1, z1)
+    assert rel(y2, y[:, :, N1:]) < 1e-13 and rel(s2, s) < 1e-13 and rel(z2, z) < 1e-13
+    sd, zd = s1, z1
+    for i in range(N1, N1 + N2):
+        yd, sd, zd = oracle.decode_step(q[:, :, i], k[:, :, i], v[:, :, i], sd, zd, gamma=gam)
+        assert rel(yd, y[:, :, i]) < 1e-13
+    assert rel(sd, s) < 1e-13 and rel(zd, z) < 1e-13
+
+
+def test_decay_outside_unit_interval_is_rejected():
+    q = rnd(1, 1, 4, 16)
+    with pytest.raises(RuntimeError):
+        oracle.prefill_decay(q, q, rnd(1, 1, 4, 8), [1.5])
+    with pytest.raises(RuntimeError):
+        oracle.prefill_decay(q, q, rnd(1, 1, 4, 8), [-0.1])
