@@ -10,6 +10,8 @@ times the other two calls of the path, reported under ``legs``:
     counts uniform in [0, M], la_prefix_prefill_padded);
   - jrt_prompt: the JRT-Prompt alternative, la_prefill over the prompt read
     twice (2N = 65536 tokens), timed against the prefix call;
+  - prefill_decay / decode_decay: the long-prefill and decode workloads with a
+    fixed per-head decay 1 - 2^-(4+h) (la_prefill_decay, la_decode_step_decay);
   - decode: la_decode_step on B=128, H=16, 512 consecutive steps captured in
     one CUDA graph, state from a 2048-token prefill (tokens/s and HBM GB/s).
 Inputs are seeded synthetic tensors already resident in HBM and larger than
@@ -365,7 +367,37 @@ def leg_jrt_prompt(la, args, dist, dev):
     return {"ms": ms, "B": B, "H": H, "N": w.N, "N_read": N2}
 
 
-def leg_decode(la, args, dist, dev):
+def decay_rates(H: int, dev) -> torch.Tensor:
+    """Per-head decay rates 1 - 2^-(4 + h) (from 0.9375 to nearly 1)."""
+    return torch.tensor([1.0 - 2.0 ** -(4 + h) for h in range(H)], dtype=torch.float32, device=dev)
+
+
+def leg_prefill_decay(la, args, dist, dev):
+    """The long-prefill workload with a fixed per-head decay (la_prefill_decay)."""
+    w = inputs.WORKLOADS[3]
+    B, H, N = w.B, w.H, w.N
+    g = torch.Generator(device=dev)
+    g.manual_seed(shard_seed(w.seed + 31, dist.rank))
+    q = gen_device((B, H, N, 16), g, dev=dev)
+    k = gen_device((B, H, N, 16), g, dev=dev)
+    v = gen_device((B, H, N, 64), g, dev=dev)
+    s0 = torch.randn((B, H, 273, 64), generator=g, device=dev)
+    z0 = torch.rand((B, H, 273), generator=g, device=dev) + 64.0
+    gam = decay_rates(H, dev)
+    y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
+    s = torch.empty_like(s0)
+    z = torch.empty_like(z0)
+
+    def step():
+        la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z, gamma=gam)
+
+    ms = time_loop(step, max(1, args.steps // 2), max(3, args.warmup // 2), dist)
+    la.check_device_status()
+    return {"ms": ms, "B": B, "H": H, "N": N}
+
+
+def leg_decode(la, args, dist, dev, decay: bool = False):
+    """512 decode steps in one CUDA graph (with decay: la_decode_step_decay)."""
     w = inputs.WORKLOADS[5]
     B, H, T = w.B, w.H, args.decode_steps
     g = torch.Generator(device=dev)
@@ -379,8 +411,9 @@ def leg_decode(la, args, dist, dev):
     kd = gen_device((T, B, H, 16), g, dev=dev)
     vd = gen_device((T, B, H, 64), g, dev=dev)
     yd = torch.empty((T, B, H, 64), dtype=torch.bfloat16, device=dev)
+    gam = decay_rates(H, dev) if decay else None
     # warm up the library (per-device set-up) before capture
-    la.decode_step(qd[0], kd[0], vd[0], s, z, y=yd[0], inplace=True)
+    la.decode_step(qd[0], kd[0], vd[0], s, z, y=yd[0], inplace=True, gamma=gam)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
@@ -388,7 +421,7 @@ def leg_decode(la, args, dist, dev):
     with torch.cuda.stream(cap):
         with torch.cuda.graph(graph, stream=cap):
             for i in range(T):
-                la.decode_step(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True)
+                la.decode_step(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True, gamma=gam)
     torch.cuda.synchronize()
     ms = time_loop(graph.replay, max(1, args.steps // 4), max(3, args.warmup // 2), dist)
     la.check_device_status()
@@ -464,7 +497,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="prefill,prefix,prefix_padded,jrt_prompt,decode")
+    ap.add_argument("--legs", default="prefill,prefix,prefix_padded,jrt_prompt,prefill_decay,decode,decode_decay")
     ap.add_argument("--decode-steps", type=int, default=512)
     ap.add_argument("--cpu-sample-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -499,8 +532,12 @@ def main():
         res["prefix_padded"] = leg_prefix_padded(la, args, dist, dev)
     if "jrt_prompt" in legs:
         res["jrt_prompt"] = leg_jrt_prompt(la, args, dist, dev)
+    if "prefill_decay" in legs:
+        res["prefill_decay"] = leg_prefill_decay(la, args, dist, dev)
     if "decode" in legs:
         res["decode"] = leg_decode(la, args, dist, dev)
+    if "decode_decay" in legs:
+        res["decode_decay"] = leg_decode(la, args, dist, dev, decay=True)
     pre["clocks"] = clocks.stop()
 
     W = dist.world
@@ -578,17 +615,30 @@ def main():
             entry["time_vs_jrt_rnn_prefix"] = r["ms"] / line["legs"]["prefix"]["ms_per_call"]
         line["legs"]["jrt_prompt"] = entry
         launches += max(1, args.steps // 4)
-    if "decode" in res:
-        r = res["decode"]
+    if "prefill_decay" in res:
+        r = res["prefill_decay"]
+        t = r["ms"] / 1e3
+        fl = r["B"] * r["H"] * r["N"] * FLOPS_PER_HEAD_TOKEN
+        line["legs"]["prefill_decay"] = {
+            "workload": inputs.WORKLOADS[3].name + "-decay-1-2^-(4+h)", "ms_per_call": r["ms"],
+            "tokens_per_s": W * r["B"] * r["N"] / t, "achieved_tflops": fl / t / 1e12,
+            "tc_frac": fl / t / 1e12 / pk["bf16_tflops"]}
+        launches += max(1, args.steps // 2)
+    for dname in ("decode", "decode_decay"):
+        if dname not in res:
+            continue
+        r = res[dname]
         per_step_ms = r["ms_per_graph"] / r["steps_per_graph"]
         bh = r["B"] * r["H"]
         by = bh * (2 * STATE_BYTES + BYTES_PER_HEAD_TOKEN_BF16)
         gbs = by / (per_step_ms / 1e3) / 1e9
-        line["legs"]["decode"] = {
-            "workload": inputs.WORKLOADS[5].name, "us_per_step": per_step_ms * 1e3,
+        line["legs"][dname] = {
+            "workload": inputs.WORKLOADS[5].name + ("-decay-1-2^-(4+h)" if dname == "decode_decay" else ""),
+            "us_per_step": per_step_ms * 1e3,
             "tokens_per_s": W * r["B"] / (per_step_ms / 1e3),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / pk["hbm_gbs"], "traffic": kernel_traffic("decode"),
+                         "frac": gbs / pk["hbm_gbs"],
+                         "traffic": kernel_traffic("decode") if dname == "decode" else None,
                          "algorithmic_bytes_per_launch": by},
             "cuda_graph_steps": r["steps_per_graph"], "finite": r["finite"]}
         launches += r["steps_per_graph"] * max(1, args.steps // 4)

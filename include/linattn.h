@@ -173,6 +173,41 @@ LA_API la_status la_prefix_prefill_padded(const void *q, const void *k, const vo
                                           la_dtype dtype, float eps, la_stream_t stream);
 
 /*
+ * la_prefill_decay, la_decode_step_decay -- the causal prefill and the decode
+ * step with a fixed per-head decay gamma_h ("Understanding and Improving
+ * Length Generalization in Recurrent Models" reading notes, sec. 2.1 Eq. (1)
+ * with A_t = gamma_h I; the BASED reading notes, sec. 2.4, mention fixed
+ * per-head decay rates in some runs):
+ *
+ *   s_i = gamma_h s_(i-1) + phi(k_i) v_i^T,   z_i = gamma_h z_(i-1) + phi(k_i),
+ *   y_i = phi(q_i)^T s_i / (phi(q_i)^T z_i + eps),   s_(-1) = s0, z_(-1) = z0
+ *
+ * so the initial state reaches position i (0-based) as gamma^(i+1) s0 (sec.
+ * 2.5, Eq. (4)).  gamma = 1 is the undecayed recurrence.
+ *
+ *   gamma  in  [H] fp32, DEVICE pointer, 4-byte aligned, required;
+ *              0 <= gamma_h <= 1.
+ *
+ * A rate outside [0, 1] (or NaN) is clamped on the device (NaN to 0) and
+ * recorded in the device status word: the next la_check_device_status
+ * returns LA_ERR_INVALID_ARG.  gamma must not overlap an output.  All other
+ * arguments, layouts and errors are those of la_prefill / la_decode_step.
+ * There is no decayed prefix call: the pages do not say how the non-causal
+ * prefix state would decay.
+ */
+LA_API la_status la_prefill_decay(const void *q, const void *k, const void *v,
+                                  const float *s0, const float *z0, const float *gamma,
+                                  void *y, float *s_out, float *z_out,
+                                  int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                                  la_dtype dtype, float eps, la_stream_t stream);
+
+LA_API la_status la_decode_step_decay(const void *q, const void *k, const void *v,
+                                      const float *gamma, const float *s_in, const float *z_in,
+                                      float *s_out, float *z_out, void *y,
+                                      int64_t B, int64_t H, int d_feat, int d_v,
+                                      la_dtype dtype, float eps, la_stream_t stream);
+
+/*
  * la_decode_step -- one recurrent decode step per (b, h) (BASED reading
  * notes, sec. 2.2 Eq. (2) for one token; sec. 2.5 notes that decoding still
  * reads and writes the whole persistent state).  The state is updated first
@@ -234,8 +269,8 @@ LA_API const char *la_status_string(la_status status);
  * library's device status word on the current device.  Returns LA_ERR_TIMEOUT
  * if any kernel since the last check gave up a bounded wait (its outputs are
  * then undefined), else LA_ERR_INVALID_ARG if a padded call met a padding
- * count outside [0, N] (it was clamped), LA_ERR_CUDA if the synchronization
- * failed, LA_OK else.
+ * count outside [0, N] or a decayed call a rate outside [0, 1] (it was
+ * clamped), LA_ERR_CUDA if the synchronization failed, LA_OK else.
  */
 LA_API la_status la_check_device_status(la_stream_t stream);
 

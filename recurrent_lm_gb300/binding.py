@@ -40,6 +40,10 @@ SIGNATURES = {
                         _I, _F, _VP]),
     "la_prefill_padded": (_I, [_VP, _VP, _VP, _FP, _FP, _VP, _VP, _FP, _FP, _I64, _I64, _I64, _I,
                                _I, _I, _F, _VP]),
+    "la_prefill_decay": (_I, [_VP, _VP, _VP, _FP, _FP, _FP, _VP, _FP, _FP, _I64, _I64, _I64, _I,
+                              _I, _I, _F, _VP]),
+    "la_decode_step_decay": (_I, [_VP, _VP, _VP, _FP, _FP, _FP, _FP, _FP, _VP, _I64, _I64, _I, _I,
+                                  _I, _F, _VP]),
     "la_prefix_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "la_prefix_prefill": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _FP, _FP, _VP,
                                _SZ, _I64, _I64, _I64, _I, _I, _I, _F, _VP]),
@@ -121,11 +125,12 @@ def _need_pad(left_pad, B):
 
 
 def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
-            z_out=None, want_state: bool = True, stream=None, left_pad=None):
+            z_out=None, want_state: bool = True, stream=None, left_pad=None, gamma=None):
     """Causal prefill (la_prefill).  q,k [B,H,N,16], v [B,H,N,64] (bf16 or fp32,
     CUDA, contiguous); s0 [B,H,273,64], z0 [B,H,273] fp32 or None.
     left_pad: CUDA int32 [B] counts of leading padding positions per batch row
-    (la_prefill_padded), or None.
+    (la_prefill_padded), or None.  gamma: CUDA fp32 [H] per-head decay in
+    [0, 1] (la_prefill_decay), or None; not combined with left_pad.
     Returns (y, s_out, z_out); the states are None when want_state is False."""
     lib = load_library()
     B, H, N, _ = q.shape
@@ -149,7 +154,14 @@ def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
     if z_out is not None:
         _need(z_out, "z_out", (B, H, D_PHI), torch.float32)
     _need_pad(left_pad, B)
-    if left_pad is None:
+    if gamma is not None:
+        if left_pad is not None:
+            raise ValueError("left_pad and gamma cannot be combined")
+        _need(gamma, "gamma", (H,), torch.float32)
+        _raise(lib.la_prefill_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(gamma),
+                                    _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q),
+                                    float(eps), _stream(stream)))
+    elif left_pad is None:
         _raise(lib.la_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
                               _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q), float(eps), _stream(stream)))
     else:
@@ -242,9 +254,10 @@ def noalloc_scratch_bytes() -> int:
 
 
 def decode_step(q, k, v, s, z, *, eps: float = 0.0, y=None, s_out=None, z_out=None,
-                inplace: bool = False, stream=None):
+                inplace: bool = False, stream=None, gamma=None):
     """One decode step (la_decode_step).  q,k [B,H,16], v [B,H,64]; s [B,H,273,64],
-    z [B,H,273] fp32.  With inplace=True the state is updated in s, z."""
+    z [B,H,273] fp32.  With inplace=True the state is updated in s, z.
+    gamma: CUDA fp32 [H] per-head decay (la_decode_step_decay), or None."""
     lib = load_library()
     B, H, _ = q.shape
     dt = q.dtype
@@ -261,9 +274,15 @@ def decode_step(q, k, v, s, z, *, eps: float = 0.0, y=None, s_out=None, z_out=No
         z_out = torch.empty_like(z)
     if y is None:
         y = torch.empty((B, H, D_V), dtype=dt, device=q.device)
-    _raise(lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(z), _ptr(s_out),
-                              _ptr(z_out), _ptr(y), B, H, D_FEAT, D_V, _dt(q), float(eps),
-                              _stream(stream)))
+    if gamma is None:
+        _raise(lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(z), _ptr(s_out),
+                                  _ptr(z_out), _ptr(y), B, H, D_FEAT, D_V, _dt(q), float(eps),
+                                  _stream(stream)))
+    else:
+        _need(gamma, "gamma", (H,), torch.float32)
+        _raise(lib.la_decode_step_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(s), _ptr(z),
+                                        _ptr(s_out), _ptr(z_out), _ptr(y), B, H, D_FEAT, D_V, _dt(q),
+                                        float(eps), _stream(stream)))
     return y, s_out, z_out
 
 

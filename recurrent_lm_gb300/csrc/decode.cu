@@ -23,11 +23,15 @@ constexpr int kColGroups = kDV / 4;              // 16 float4 per state row
 constexpr int kRowGroups = kThreads / kColGroups;  // 16
 constexpr int kRowsPerThread = (kD + kRowGroups - 1) / kRowGroups;  // 18
 
-template <typename T>
+// kDecay: s = gamma_h s + phi(k) v^T, z = gamma_h z + phi(k) (a fixed per-head
+// decay, the general recurrence of the length-generalization notes, sec. 2.1
+// Eq. (1), with A_t = gamma I); a separate instantiation.
+template <typename T, bool kDecay>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
                    const T *__restrict__ v, const float *s_in, const float *z_in,
-                   float *s_out, float *z_out, T *__restrict__ y, float eps) {
+                   float *s_out, float *z_out, T *__restrict__ y, float eps,
+                   const float *__restrict__ gamma, int64_t H, unsigned *status) {
     __shared__ float xq[kDFeat], xk[kDFeat];
     __shared__ float phq[kD + 15], phk[kD + 15];
     __shared__ float4 red[kRowGroups][kColGroups];
@@ -35,6 +39,14 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
 
     const int64_t bh = blockIdx.x;
     const int tid = threadIdx.x;
+    float g = 1.f;
+    if constexpr (kDecay) {
+        g = gamma[bh % H];
+        if (!(g >= 0.f && g <= 1.f)) {  // clamped; reported by one thread
+            if (tid == 0) atomicOr(status, kStatusBadDecay);
+            g = (g > 1.f) ? 1.f : 0.f;
+        }
+    }
     if (tid < kDFeat) xq[tid] = 0.5f * Act<T>::load(q, bh * kDFeat + tid);
     else if (tid < 2 * kDFeat) xk[tid - kDFeat] = 0.5f * Act<T>::load(k, bh * kDFeat + tid - kDFeat);
 
@@ -68,12 +80,12 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
     // z update and the normaliser phi(q).z_new.
     float dpart = 0.f;
     {
-        const float zn = zin0 + phk[tid];
+        const float zn = (kDecay ? g * zin0 : zin0) + phk[tid];
         z_out[bh * kD + tid] = zn;
         dpart = phq[tid] * zn;
         if (tid + kThreads < kD) {
             const int f = tid + kThreads;
-            const float zn1 = zin1 + phk[f];
+            const float zn1 = (kDecay ? g * zin1 : zin1) + phk[f];
             z_out[bh * kD + f] = zn1;
             dpart += phq[f] * zn1;
         }
@@ -90,6 +102,12 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
         if (r < kD) {
             const float pk = phk[r], pq = phq[r];
             float4 s = sr[j];
+            if constexpr (kDecay) {
+                s.x *= g;
+                s.y *= g;
+                s.z *= g;
+                s.w *= g;
+            }
             s.x = fmaf(pk, vv.x, s.x);
             s.y = fmaf(pk, vv.y, s.y);
             s.z = fmaf(pk, vv.z, s.z);
@@ -125,15 +143,16 @@ cudaError_t launch_decode(const DecodeArgs &a, la_dtype dt, cudaStream_t st) {
     const int64_t BH = a.B * a.H;
     if (BH == 0) return cudaSuccess;
     dim3 grid((unsigned)BH), block(kThreads);
-    if (dt == LA_DTYPE_BF16)
-        decode_step_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(
-            (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k,
-            (const __nv_bfloat16 *)a.v, a.s_in, a.z_in, a.s_out, a.z_out,
-            (__nv_bfloat16 *)a.y, a.eps);
-    else
-        decode_step_kernel<float><<<grid, block, 0, st>>>(
-            (const float *)a.q, (const float *)a.k, (const float *)a.v, a.s_in,
-            a.z_in, a.s_out, a.z_out, (float *)a.y, a.eps);
+    if (dt == LA_DTYPE_BF16) {
+        auto kern = a.gamma ? decode_step_kernel<__nv_bfloat16, true> : decode_step_kernel<__nv_bfloat16, false>;
+        kern<<<grid, block, 0, st>>>((const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k,
+                                     (const __nv_bfloat16 *)a.v, a.s_in, a.z_in, a.s_out, a.z_out,
+                                     (__nv_bfloat16 *)a.y, a.eps, a.gamma, a.H, a.status);
+    } else {
+        auto kern = a.gamma ? decode_step_kernel<float, true> : decode_step_kernel<float, false>;
+        kern<<<grid, block, 0, st>>>((const float *)a.q, (const float *)a.k, (const float *)a.v, a.s_in,
+                                     a.z_in, a.s_out, a.z_out, (float *)a.y, a.eps, a.gamma, a.H, a.status);
+    }
     return cudaGetLastError();
 }
 

@@ -140,7 +140,7 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 la_status prefill_impl(const void *q, const void *k, const void *v, const float *s0,
                        const float *z0, const int32_t *left_pad, void *y, float *s_out,
                        float *z_out, int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
-                       la_dtype dtype, float eps, la_stream_t stream) {
+                       la_dtype dtype, float eps, la_stream_t stream, const float *gamma = nullptr) {
     la_status st = check_common(B, H, N, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
     if ((s0 == nullptr) != (z0 == nullptr)) return LA_ERR_INVALID_ARG;
@@ -156,14 +156,14 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
     const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * kD * kDV},
                          {z_out, sizeof(float) * BH * kD}};
     if (any_overlap(in, 5, out, 3)) return LA_ERR_INVALID_ARG;
-    if (left_pad && !aligned4(left_pad)) return LA_ERR_MISALIGNED;
-    if (overlaps({left_pad, sizeof(int32_t) * B}, out[0]) || overlaps({left_pad, sizeof(int32_t) * B}, out[1]) ||
-        overlaps({left_pad, sizeof(int32_t) * B}, out[2]))
-        return LA_ERR_INVALID_ARG;
+    if ((left_pad && !aligned4(left_pad)) || (gamma && !aligned4(gamma))) return LA_ERR_MISALIGNED;
+    for (const Range &o : out)
+        if (overlaps({left_pad, sizeof(int32_t) * B}, o) || overlaps({gamma, sizeof(float) * H}, o))
+            return LA_ERR_INVALID_ARG;
     int dev;
     unsigned *status;
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
-    la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad};
+    la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad, gamma};
     return to_status(run_prefill(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -274,10 +274,14 @@ la_status la_prefix_prefill_padded(const void *q, const void *k, const void *v, 
                        workspace_bytes, B, H, N, d_feat, d_v, dtype, eps, stream);
 }
 
-la_status la_decode_step(const void *q, const void *k, const void *v, const float *s_in,
-                         const float *z_in, float *s_out, float *z_out, void *y, int64_t B,
-                         int64_t H, int d_feat, int d_v, la_dtype dtype, float eps,
-                         la_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+la_status decode_impl(const void *q, const void *k, const void *v, const float *gamma,
+                      const float *s_in, const float *z_in, float *s_out, float *z_out, void *y,
+                      int64_t B, int64_t H, int d_feat, int d_v, la_dtype dtype, float eps,
+                      la_stream_t stream) {
     la_status st = check_common(B, H, 1, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
     if (!q || !k || !v || !s_in || !z_in || !s_out || !z_out || !y) return LA_ERR_INVALID_ARG;
@@ -296,11 +300,46 @@ la_status la_decode_step(const void *q, const void *k, const void *v, const floa
     // an in-place state must not overlap the other state buffer or y either
     if (s_out == s_in && (overlaps({s_in, sb}, {z_in, zb}) || overlaps({s_in, sb}, {y, es * BH * kDV})))
         return LA_ERR_INVALID_ARG;
+    if (gamma) {
+        if (!aligned4(gamma)) return LA_ERR_MISALIGNED;
+        for (const Range &o : out)
+            if (overlaps({gamma, sizeof(float) * H}, o)) return LA_ERR_INVALID_ARG;
+    }
     int dev;
     unsigned *status;
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
-    la::DecodeArgs a{q, k, v, s_in, z_in, s_out, z_out, y, B, H, eps};
+    la::DecodeArgs a{q, k, v, s_in, z_in, s_out, z_out, y, B, H, eps, gamma, status};
     return to_status(la::launch_decode(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status la_decode_step(const void *q, const void *k, const void *v, const float *s_in,
+                         const float *z_in, float *s_out, float *z_out, void *y, int64_t B,
+                         int64_t H, int d_feat, int d_v, la_dtype dtype, float eps,
+                         la_stream_t stream) {
+    return decode_impl(q, k, v, nullptr, s_in, z_in, s_out, z_out, y, B, H, d_feat, d_v, dtype, eps,
+                       stream);
+}
+
+la_status la_decode_step_decay(const void *q, const void *k, const void *v, const float *gamma,
+                               const float *s_in, const float *z_in, float *s_out, float *z_out,
+                               void *y, int64_t B, int64_t H, int d_feat, int d_v, la_dtype dtype,
+                               float eps, la_stream_t stream) {
+    if (!gamma) return LA_ERR_INVALID_ARG;
+    return decode_impl(q, k, v, gamma, s_in, z_in, s_out, z_out, y, B, H, d_feat, d_v, dtype, eps,
+                       stream);
+}
+
+la_status la_prefill_decay(const void *q, const void *k, const void *v, const float *s0,
+                           const float *z0, const float *gamma, void *y, float *s_out,
+                           float *z_out, int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                           la_dtype dtype, float eps, la_stream_t stream) {
+    if (!gamma) return LA_ERR_INVALID_ARG;
+    return prefill_impl(q, k, v, s0, z0, nullptr, y, s_out, z_out, B, H, N, d_feat, d_v, dtype, eps,
+                        stream, gamma);
 }
 
 la_status la_check_device_status(la_stream_t stream) {

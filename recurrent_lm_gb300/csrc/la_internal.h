@@ -18,6 +18,7 @@ constexpr int kStateFloats = kD * kDV + kD;  // one head's s and z
 // Bits of the device status word (one per failure class).
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusBadPad = 2u;   // a left-padding count outside [0, N] (clamped)
+constexpr unsigned kStatusBadDecay = 4u; // a decay rate outside [0, 1] (clamped)
 
 // Leading padding positions of batch row b: left_pad[b] clamped to [0, N]
 // (NULL: none).  An out-of-range count sets kStatusBadPad (by one thread).
@@ -41,6 +42,7 @@ struct PrefillArgs {
     float eps;
     unsigned *status;   // device status word
     const int32_t *left_pad;  // [B] leading padding positions per batch row, or NULL
+    const float *gamma;       // [H] per-head decay in [0, 1], or NULL (no decay)
 };
 
 struct DecodeArgs {
@@ -50,6 +52,8 @@ struct DecodeArgs {
     void *y;
     int64_t B, H;
     float eps;
+    const float *gamma;       // [H] per-head decay in [0, 1], or NULL (no decay)
+    unsigned *status;
 };
 
 // Per-segment partial prefix states: part_s [BH][nseg][273][64],

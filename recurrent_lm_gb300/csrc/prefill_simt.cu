@@ -42,7 +42,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const float *__restrict__ z0, T *__restrict__ y,
                     float *__restrict__ s_out, float *__restrict__ z_out,
                     int64_t N, float eps, const int32_t *__restrict__ left_pad, int64_t H,
-                    unsigned *status) {
+                    unsigned *status, const float *__restrict__ gamma) {
     __shared__ float xq[kDFeat], xk[kDFeat], vs[kDV];
     __shared__ float phq[kD], phk[kD];
     __shared__ float zsh[kD];
@@ -63,6 +63,16 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
 
     // leading padding positions of this batch row: y = 0, no state change
     const int64_t lpad = row_left_pad(left_pad, bh / H, N, status, tid == 0);
+    // per-head decay (s = gamma s + phi(k) v^T), clamped to [0, 1] and reported
+    const bool decay = gamma != nullptr;
+    float gam = 1.f;
+    if (decay) {
+        gam = gamma[bh % H];
+        if (!(gam >= 0.f && gam <= 1.f)) {
+            if (tid == 0) atomicOr(status, kStatusBadDecay);
+            gam = (gam > 1.f) ? 1.f : 0.f;
+        }
+    }
     for (int64_t i = 0; i < lpad; ++i)
         if (tid < kDV) Act<T>::store(y, (bh * N + i) * kDV + tid, 0.f);
     for (int64_t i = lpad; i < N; ++i) {
@@ -74,7 +84,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
             const float pk = phi_feature(xk, f), pq = phi_feature(xq, f);
             phk[f] = pk;
             phq[f] = pq;
-            const float zn = zsh[f] + pk;
+            const float zn = (decay ? gam * zsh[f] : zsh[f]) + pk;
             zsh[f] = zn;
             dpart = fmaf(pq, zn, dpart);
         }
@@ -88,7 +98,7 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
         for (int j = 0; j < kRowsPerThread; ++j) {
             const int r = g + j * kRowGroups;
             if (r < kD) {
-                s[j] = fmaf(phk[r], vc, s[j]);
+                s[j] = fmaf(phk[r], vc, decay ? gam * s[j] : s[j]);
                 acc = fmaf(phq[r], s[j], acc);
             }
         }
@@ -226,11 +236,11 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, la_dtype dt, cudaStream_t 
         prefill_simt_kernel<__nv_bfloat16><<<(unsigned)BH, kThreads, 0, st>>>(
             (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k,
             (const __nv_bfloat16 *)a.v, a.s0, a.z0, (__nv_bfloat16 *)a.y, a.s_out,
-            a.z_out, a.N, a.eps, a.left_pad, a.H, a.status);
+            a.z_out, a.N, a.eps, a.left_pad, a.H, a.status, a.gamma);
     else
         prefill_simt_kernel<float><<<(unsigned)BH, kThreads, 0, st>>>(
             (const float *)a.q, (const float *)a.k, (const float *)a.v, a.s0, a.z0,
-            (float *)a.y, a.s_out, a.z_out, a.N, a.eps, a.left_pad, a.H, a.status);
+            (float *)a.y, a.s_out, a.z_out, a.N, a.eps, a.left_pad, a.H, a.status, a.gamma);
     return cudaGetLastError();
 }
 

@@ -68,7 +68,8 @@ constexpr uint32_t kSmK = 194560;      // 3 x [128][16] bf16 SW32
 constexpr uint32_t kSmY = 206848;      // 4 x [32 rows][64] bf16 SW128: y staging for TMA stores
 constexpr uint32_t kSmRows = kSmY + 16384;  // [160] x int4 feature -> ABI row table
 constexpr uint32_t kSmBar = kSmRows + 160 * 16;
-constexpr uint32_t kSmTotal = kSmBar + 512;
+constexpr uint32_t kSmPow = kSmBar + 512;  // decay: [129] float2 (gamma^d, gamma^(d-1))
+constexpr uint32_t kSmTotal = kSmPow + 1280;
 constexpr uint32_t kSmAlloc = kSmTotal + 1024;
 constexpr int kStages = 3;
 
@@ -113,8 +114,12 @@ __device__ __forceinline__ void write_sb_group(uint32_t sbase, int d, int g, con
 // bf16 operand rows of the state after a chunk, for one warp's TMEM lanes and
 // feature groups [kG0, kG0 + kNG) (32 features each): value rows d < 64 and
 // the z' row 64 (lane 0 of the warp owning lanes 64..95).
-template <int kG0, int kNG>
-__device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, int d, bool zrow, int lane) {
+// With kDecay the fp32 state in TMEM is then multiplied by `decay` (gamma to
+// the next chunk's length) for the next update, while the operand keeps the
+// undecayed state that the next read-out needs.
+template <int kG0, int kNG, bool kDecay = false>
+__device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, int d, bool zrow, int lane,
+                                               float decay = 1.f) {
     uint32_t r[32 * kNG];
     if constexpr (kNG == 2) {
         uint32_t (&r64)[64] = reinterpret_cast<uint32_t (&)[64]>(r);
@@ -123,10 +128,21 @@ __device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, i
         uint32_t (&r32)[32] = reinterpret_cast<uint32_t (&)[32]>(r);
         tmem_load32_sync(taddr + 32 * kG0, r32);
     }
-    if (zrow && lane != 0) return;
+    if (!zrow || lane == 0) {
 #pragma unroll
-    for (int g = 0; g < kNG; ++g)
-        write_sb_group(sbase, zrow ? 64 : d, kG0 + g, *reinterpret_cast<const uint32_t (*)[32]>(r + 32 * g));
+        for (int g = 0; g < kNG; ++g)
+            write_sb_group(sbase, zrow ? 64 : d, kG0 + g, *reinterpret_cast<const uint32_t (*)[32]>(r + 32 * g));
+    }
+    if constexpr (kDecay) {
+        __syncwarp();  // tcgen05.st is warp-collective
+#pragma unroll
+        for (int g = 0; g < kNG; ++g) {
+            uint32_t w[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(__uint_as_float(r[32 * g + j]) * decay);
+            tmem_store32_sync(taddr + 32 * (kG0 + g), w);
+        }
+    }
 }
 
 // Optional per-role timeline of CTA 0 (compile with -DLA_TRACE): SM clock
@@ -144,14 +160,20 @@ __device__ uint32_t g_trace[5][kTraceChunks][8];
 #endif
 enum { TR_TMA = 0, TR_MMA, TR_GEN, TR_EPI, TR_CONV };
 
-// kPad: the launch carries per-row left-padding counts (a separate
-// instantiation, so the unpadded kernel carries none of the masking code).
-template <bool kPad>
+// kPad: the launch carries per-row left-padding counts; kDecay: a per-head
+// decay gamma (s_i = gamma s_(i-1) + phi(k_i) v_i^T).  Separate instantiations,
+// so the plain kernel carries none of their code.  With decay, token t of a
+// chunk of length L reads gamma^(t+1) Phi'_Q . S (scaled query features),
+// writes gamma^(L-1-t) Phi'_K (scaled key features), the intra-chunk kernel
+// entries carry gamma^(i-j), and the state is multiplied by gamma^L in TMEM
+// before each update.
+template <bool kPad, bool kDecay>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty,
                   const float *__restrict__ s0,
-                  const float *__restrict__ z0, const int32_t *__restrict__ left_pad, int64_t H,
+                  const float *__restrict__ z0, const int32_t *__restrict__ left_pad,
+                  const float *__restrict__ gamma, int64_t H,
                   float *__restrict__ s_out, float *__restrict__ z_out, int N, float eps,
                   unsigned *status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -219,6 +241,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kSmTmemSlot);
 
+    // decay: the head's gamma (clamped to [0, 1]; out of range is reported) and
+    // its powers (gamma^d, gamma^(d-1)) for d = 0..128
+    auto pow_gamma = [&](int d) { return kDecay ? reinterpret_cast<const float2 *>(smem + kSmPow)[d].x : 1.f; };
+    if constexpr (kDecay) {
+        float g = gamma[bh % H];
+        if (!(g >= 0.f && g <= 1.f)) {
+            if (tid == 0) atomicOr(status, kStatusBadDecay);
+            g = (g > 1.f) ? 1.f : 0.f;
+        }
+        if (tid <= 128)
+            reinterpret_cast<float2 *>(smem + kSmPow)[tid] =
+                make_float2(powf(g, (float)tid), tid > 0 ? powf(g, (float)(tid - 1)) : 0.f);
+        __syncthreads();
+    }
+    // length of chunk c (the last may be short)
+    auto chunk_len = [&](int c) { return min(kC, N - c * kC); };
+    // the antisymmetric part of s0 bypasses the compact state: it decays by gamma^N
+    const float anti_decay = kDecay ? powf(pow_gamma(1), (float)N) : 1.f;
+
     // initial state, before any role starts: S'^T rows (values d = 0..63, lanes of
     // warps 12, 13) and z' (lanes 64.., warp 14) in TMEM, and their bf16 operand rows
     if (warp >= 12 && warp < 15) {
@@ -233,8 +274,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             uint32_t r[32];
             compact_initial_group(col0, stride, rows_tab + 32 * g, r);
             __syncwarp();
-            tmem_store32_sync(tmem + lanebase + kTmS + 32 * g, r);
             if (!zrow || lane == 0) write_sb_group(sb + kSmSb, zrow ? 64 : d, g, r);
+            if constexpr (kDecay) {  // the first update starts from gamma^L0 s0
+                const float d0 = pow_gamma(chunk_len(0));
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * d0);
+            }
+            tmem_store32_sync(tmem + lanebase + kTmS + 32 * g, r);
         }
         fence_async_smem();
         tc_fence_before();
@@ -381,7 +427,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (lane == 0) mbar_arrive(bar(B_QK_EMPTY + st));
             // the read-out of chunk c - 1 (NUM_FULL) released the Phi'_Q buffer
             if (!mbar_wait(bar(B_NUM_FULL), pc ^ 1u, abort, status)) break;
-            emit_features<false>(qlo, qhi, sb + kSmPhiQ, t, false, std::make_integer_sequence<int, 20>{});
+            if constexpr (kDecay) {  // token t reads gamma^(t+1) of the state before the chunk
+                const float lq = pow_gamma(t + 1);
+                emit_features<false, true>(qlo, qhi, sb + kSmPhiQ, t, false, std::make_integer_sequence<int, 20>{},
+                                           pack_bf16(lq, lq));
+            } else {
+                emit_features<false>(qlo, qhi, sb + kSmPhiQ, t, false, std::make_integer_sequence<int, 20>{});
+            }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PHQ_FULL));
@@ -393,7 +445,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (!mbar_wait(bar(B_S_FULL), pc ^ 1u, abort, status)) break;
             if (c > 0 && tid == 128) mbar_arrive(bar(B_V_EMPTY + (c - 1) % kStages));
             if (tid == 128) LA_TR(TR_GEN, c, 2);
-            emit_features<true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
+            if constexpr (kDecay) {  // token t enters the state after the chunk with gamma^(L-1-t)
+                const float lk = pow_gamma(max(chunk_len(c) - 1 - t, 0));
+                emit_features<true, true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{},
+                                          pack_bf16(lk, lk));
+            } else {
+                emit_features<true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
+            }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PHK_FULL));
@@ -429,7 +487,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
-                        const uint64_t p2 = ffma2(t2, ffma2(t2, c32, c4), c1);
+                        uint64_t p2 = ffma2(t2, ffma2(t2, c32, c4), c1);
+                        if constexpr (kDecay) {  // times (gamma^(i-j), gamma^(i-j-1)); j > i is masked below
+                            const int dd = max(i - (64 * pp + 2 * j), 0);
+                            const float2 f = reinterpret_cast<const float2 *>(smem + kSmPow)[dd];
+                            p2 = fmul2(p2, f2pack(f.x, f.y));
+                        }
                         float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
                         if (diag) {
                             const int key = 64 * pp + 2 * j;
@@ -468,9 +531,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tc_fence_after();
                 const bool last = (c == n - 1);
                 if (w < 3) {
-                    if (!last) convert_groups<3, 2>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane);
+                    if (!last)
+                        convert_groups<3, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane,
+                                                     pow_gamma(chunk_len(c + 1)));
                     else store_final_groups(tmem + lanebase + kTmS, 3, 2, i, zrow, lane, rows_tab, s0h,
-                                            s_outh, z0h, z_outh);
+                                            s_outh, z0h, z_outh, anti_decay);
                 }
                 __syncwarp();
                 if (!last) {
@@ -534,12 +599,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             const bool last = (c == n - 1);
             if (w < 3) {
                 if (!last) {
-                    convert_groups<0, 2>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane);
+                    const float dn = pow_gamma(chunk_len(c + 1));
+                    convert_groups<0, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                     __syncwarp();
-                    convert_groups<2, 1>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane);
+                    convert_groups<2, 1, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                 } else {
                     store_final_groups(tmem + lanebase + kTmS, 0, 3, i, zrow, lane, rows_tab, s0h, s_outh,
-                                       z0h, z_outh);
+                                       z0h, z_outh, anti_decay);
                 }
                 __syncwarp();
             }
@@ -619,20 +685,27 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<false>,
+        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<false, false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(prefill_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmAlloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kSmAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
+    if (a.left_pad && a.gamma) return cudaErrorInvalidValue;  // no padded decayed variant
     if (a.left_pad)
-        prefill_tc_kernel<true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, a.left_pad, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+        prefill_tc_kernel<true, false><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
+            tq, tk, tv, ty, a.s0, a.z0, a.left_pad, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+    else if (a.gamma)
+        prefill_tc_kernel<false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
+            tq, tk, tv, ty, a.s0, a.z0, nullptr, a.gamma, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
     else
-        prefill_tc_kernel<false><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+        prefill_tc_kernel<false, false><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
+            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
     return cudaGetLastError();
 }
 

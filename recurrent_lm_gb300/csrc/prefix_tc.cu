@@ -161,7 +161,7 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
             if (ok && n > 0) {
                 const int64_t slot = bh * nseg + seg;
                 store_final_groups(tmem + ((uint32_t)(32 * w) << 16), 0, kNFeat / 32, 32 * w + lane, zrow, lane,
-                                   rows_tab, nullptr, part_s + slot * kD * kDV, nullptr, part_z + slot * kD);
+                                   rows_tab, nullptr, part_s + slot * kD * kDV, nullptr, part_z + slot * kD, 1.f);
             }
         }
     }

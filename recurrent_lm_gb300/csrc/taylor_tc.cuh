@@ -65,23 +65,27 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t x, uint32_t y) {
 }
 
 // Packed features of one token: X[j] = (xbar_2j, xbar_2j+1) as bf16x2, Y[j] =
-// (xbar_2j+1, xbar_2j+2), H[j] = X[j] / 2 (keys only).
+// (xbar_2j+1, xbar_2j+2), H[j] = X[j] / 2 (keys only).  XL[j] is the left
+// factor of every product: X[j] itself, or X[j] times a per-token scale when
+// the whole feature vector is scaled (then cst = (scale, 0) is the constant
+// feature), so scaling costs 8 multiplies instead of 80.
 template <bool kKey, int R>
-__device__ __forceinline__ uint32_t feat_pair(const uint32_t (&X)[8], const uint32_t (&Y)[7],
-                                              const uint32_t (&H)[8], uint32_t b15) {
+__device__ __forceinline__ uint32_t feat_pair(const uint32_t (&XL)[8], const uint32_t (&X)[8],
+                                              const uint32_t (&Y)[7], const uint32_t (&H)[8],
+                                              uint32_t b15, uint32_t cst) {
     constexpr PairSpec p = pair_spec(R);
     if constexpr (p.kind == 0) {
-        if constexpr (kKey) return hmul2(X[p.j], H[p.j]);
-        else return hmul2(X[p.j], X[p.j]);
+        if constexpr (kKey) return hmul2(XL[p.j], H[p.j]);
+        else return hmul2(XL[p.j], X[p.j]);
     } else if constexpr (p.kind == 1) {
-        if constexpr (p.d % 2 == 0) return hmul2(X[p.j], X[p.j + p.d / 2]);
-        else return hmul2(X[p.j], Y[p.j + (p.d - 1) / 2]);
+        if constexpr (p.d % 2 == 0) return hmul2(XL[p.j], X[p.j + p.d / 2]);
+        else return hmul2(XL[p.j], Y[p.j + (p.d - 1) / 2]);
     } else if constexpr (p.kind == 2) {
-        return hmul2(__byte_perm(X[2 * p.j], X[2 * p.j + 1], 0x5410), b15);
+        return hmul2(__byte_perm(XL[2 * p.j], XL[2 * p.j + 1], 0x5410), b15);
     } else if constexpr (p.kind == 3) {
-        return X[p.j];
+        return XL[p.j];
     } else if constexpr (p.kind == 4) {
-        return 0x00003F80u;  // (1.0, 0)
+        return cst;  // (1.0, 0), or (scale, 0)
     } else {
         return 0u;
     }
@@ -100,20 +104,23 @@ __device__ __forceinline__ uint32_t feat_chunk_off(int J, int t) {
 }
 
 template <bool kKey, int J>
-__device__ __forceinline__ void emit_chunk(const uint32_t (&X)[8], const uint32_t (&Y)[7],
-                                           const uint32_t (&H)[8], uint32_t b15, uint32_t base, int t,
-                                           bool zero) {
-    uint32_t w0 = feat_pair<kKey, 4 * J + 0>(X, Y, H, b15);
-    uint32_t w1 = feat_pair<kKey, 4 * J + 1>(X, Y, H, b15);
-    uint32_t w2 = feat_pair<kKey, 4 * J + 2>(X, Y, H, b15);
-    uint32_t w3 = feat_pair<kKey, 4 * J + 3>(X, Y, H, b15);
+__device__ __forceinline__ void emit_chunk(const uint32_t (&XL)[8], const uint32_t (&X)[8],
+                                           const uint32_t (&Y)[7], const uint32_t (&H)[8], uint32_t b15,
+                                           uint32_t cst, uint32_t base, int t, bool zero) {
+    uint32_t w0 = feat_pair<kKey, 4 * J + 0>(XL, X, Y, H, b15, cst);
+    uint32_t w1 = feat_pair<kKey, 4 * J + 1>(XL, X, Y, H, b15, cst);
+    uint32_t w2 = feat_pair<kKey, 4 * J + 2>(XL, X, Y, H, b15, cst);
+    uint32_t w3 = feat_pair<kKey, 4 * J + 3>(XL, X, Y, H, b15, cst);
     if (zero) w0 = w1 = w2 = w3 = 0u;
     st_shared_v4(base + feat_chunk_off<kKey>(J, t), w0, w1, w2, w3);
 }
 
-template <bool kKey, int... J>
+// Feature vector of one token into its row of the feature tile; with kScaled
+// every feature is multiplied by scale2 (a bf16x2 pair of the same scale).
+template <bool kKey, bool kScaled = false, int... J>
 __device__ __forceinline__ void emit_features(const uint4 &lo, const uint4 &hi, uint32_t base, int t,
-                                              bool zero, std::integer_sequence<int, J...>) {
+                                              bool zero, std::integer_sequence<int, J...>,
+                                              uint32_t scale2 = 0x3F803F80u) {
     // xbar = x / 2 (exact), its odd-shifted pairs, and halves for the key squares
     const uint32_t raw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     uint32_t X[8], Y[7], H[8];
@@ -124,7 +131,15 @@ __device__ __forceinline__ void emit_features(const uint4 &lo, const uint4 &hi, 
 #pragma unroll
     for (int j = 0; j < 8; ++j) H[j] = kKey ? hmul2(X[j], 0x3F003F00u) : 0u;
     const uint32_t b15 = __byte_perm(X[7], X[7], 0x3232);
-    (emit_chunk<kKey, J>(X, Y, H, b15, base, t, zero), ...);
+    if constexpr (kScaled) {
+        uint32_t XL[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) XL[j] = hmul2(X[j], scale2);
+        const uint32_t cst = scale2 & 0xFFFFu;
+        (emit_chunk<kKey, J>(XL, X, Y, H, b15, cst, base, t, zero), ...);
+    } else {
+        (emit_chunk<kKey, J>(X, X, Y, H, b15, 0x00003F80u, base, t, zero), ...);
+    }
 }
 
 // Raw token row t (16 bf16 as two 16-byte halves) of a [128][16] SW32 tile.
@@ -198,7 +213,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // CTA, so it is kept out of line.
 static __device__ __noinline__ void store_final_groups(uint32_t taddr, int g0, int ng, int d, bool zrow, int lane,
                                                        const int4 *rows_tab, const float *s0h, float *s_outh,
-                                                       const float *z0h, float *z_outh) {
+                                                       const float *z0h, float *z_outh, float anti_scale) {
     const float *col0 = zrow ? z0h : (s0h ? s0h + d : nullptr);
     float *out = zrow ? z_outh : (s_outh ? s_outh + d : nullptr);
     const int64_t stride = zrow ? 1 : kDV;
@@ -219,7 +234,8 @@ static __device__ __noinline__ void store_final_groups(uint32_t taddr, int g0, i
                     b[j] = __ldg(col0 + r2 * stride);
                 }
 #pragma unroll
-                for (int j = 0; j < 32; ++j) anti[j] = rows_tab[32 * g + j].z == 1 ? 0.5f * (a[j] - b[j]) : 0.f;
+                for (int j = 0; j < 32; ++j)
+                    anti[j] = rows_tab[32 * g + j].z == 1 ? (0.5f * anti_scale) * (a[j] - b[j]) : 0.f;
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) anti[j] = 0.f;
