@@ -77,8 +77,12 @@ constexpr int kStages = 3;
 enum {
     B_QK_FULL = 0, B_QK_EMPTY = 3, B_V_FULL = 6, B_V_EMPTY = 9,
     B_T_FULL = 12,   // [2] per T buffer
-    B_P_FULL = 14, B_PHQ_FULL, B_PHK_FULL,
-    B_NUM_FULL, B_NUM_EMPTY, B_S_FULL, B_SB_FULL, B_FINAL,
+    // PV_READY(c): P(c) (P warps) and num drained after chunk c - 1 (y warps);
+    // RO_READY(c): Phi'_Q(c) (gen warps) and the state operand after chunk c - 1
+    // (conversion warps).  Merged so the MMA issuer waits once for each: its
+    // waits are expensive after MMA issue.
+    B_PV_READY = 14, B_RO_READY, B_PHK_FULL,
+    B_NUM_FULL, B_S_FULL, B_FINAL,
     B_COUNT
 };
 constexpr uint32_t kSmTmemSlot = kSmBar + 8 * B_COUNT;
@@ -209,13 +213,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_T_FULL + i), 1);
         }
-        mbar_init(bar(B_P_FULL), 4);
-        mbar_init(bar(B_PHQ_FULL), 4);
+        mbar_init(bar(B_PV_READY), 4 + 4);
+        mbar_init(bar(B_RO_READY), 4 + 8);
         mbar_init(bar(B_PHK_FULL), 4);
         mbar_init(bar(B_NUM_FULL), 1);
-        mbar_init(bar(B_NUM_EMPTY), 4);
         mbar_init(bar(B_S_FULL), 1);
-        mbar_init(bar(B_SB_FULL), 8);
         mbar_init(bar(B_FINAL), 1);
         *abort = 0;
         mbar_init_fence();
@@ -320,8 +322,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
         }
     } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (lane == 0) {
+        // ================= MMA issuer (the whole warp; one elected lane issues) =================
+        {
+            // every wait's result is made warp-uniform so the warp stays converged
+            auto wwait = [&](uint32_t b_, uint32_t par) {
+                return __all_sync(0xffffffffu, mbar_wait(b_, par, abort, status));
+            };
             // descriptor bases; per-step offsets are added in 16-byte units
             const uint64_t dQ = smem_desc(sb + kSmQ, 16, 256, kSw32);
             const uint64_t dK = smem_desc(sb + kSmK, 16, 256, kSw32);
@@ -338,10 +344,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             };
             auto issue_qk = [&](int c) {  // T[c & 1] = Q_c K_c^T
                 const int st = c % kStages;
-                mma_bf16(tmem + tm_t(c & 1), dQ + st * (4096 >> 4), dK + st * (4096 >> 4), kIdQK, 0);
-                mma_commit(bar(B_T_FULL + (c & 1)));  // also frees the q, k stage (P epilogue forwards it)
+                mma_bf16_warp(tmem + tm_t(c & 1), dQ + st * (4096 >> 4), dK + st * (4096 >> 4), kIdQK, 0);
+                mma_commit_warp(bar(B_T_FULL + (c & 1)));  // also frees the q, k stage (P epilogue forwards it)
             };
-            bool ok = mbar_wait(bar(B_QK_FULL + 0), 0, abort, status);
+            bool ok = wwait(bar(B_QK_FULL + 0), 0);
             if (ok) {
                 tc_fence_after();
                 issue_qk(0);
@@ -353,49 +359,47 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 // P(c) is in T[b]; V(c) is in; num was drained for chunk c - 1 (which
                 // also means P V of chunk c - 1 completed: the read-out commit covers
                 // every earlier MMA, so T[b ^ 1] may take Q K^T(c + 1)); q, k of c + 1
-                ok = mbar_wait(bar(B_P_FULL), pc, abort, status) &&
-                     mbar_wait(bar(B_V_FULL + vs), (uint32_t)(c / kStages) & 1u, abort, status) &&
-                     mbar_wait(bar(B_NUM_EMPTY), pc ^ 1u, abort, status) &&
-                     (c + 1 >= n || mbar_wait(bar(B_QK_FULL + (c + 1) % kStages),
-                                              (uint32_t)((c + 1) / kStages) & 1u, abort, status));
+                ok = wwait(bar(B_PV_READY), pc) && wwait(bar(B_V_FULL + vs), (uint32_t)(c / kStages) & 1u) &&
+                     (c + 1 >= n || wwait(bar(B_QK_FULL + (c + 1) % kStages), (uint32_t)((c + 1) / kStages) & 1u));
                 if (!ok) break;
-                LA_TR(TR_MMA, c, 0);
+                if (lane == 0) LA_TR(TR_MMA, c, 0);
                 tc_fence_after();
                 if (c + 1 < n) issue_qk(c + 1);
-                LA_TR(TR_MMA, c, 1);
+                if (lane == 0) LA_TR(TR_MMA, c, 1);
                 // intra-chunk: [num | den] = P [V | 1], P from TMEM
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_bf16_ts(tmem + kTmNum, tmem + tm_t(b) + 8 * s, dV + s * (2048 >> 4), kIdPV, s > 0);
+                    mma_bf16_ts_warp(tmem + kTmNum, tmem + tm_t(b) + 8 * s, dV + s * (2048 >> 4), kIdPV, s > 0);
                 // inter-chunk read-out operands: the state after chunk c - 1, Phi'_Q(c)
-                ok = mbar_wait(bar(B_SB_FULL), pc, abort, status) && mbar_wait(bar(B_PHQ_FULL), pc, abort, status);
+                ok = wwait(bar(B_RO_READY), pc);
                 if (!ok) break;
-                LA_TR(TR_MMA, c, 2);
+                if (lane == 0) LA_TR(TR_MMA, c, 2);
                 tc_fence_after();
                 // inter-chunk read-out: [num | den] += Phi'_Q [S' | z'] (both K-major)
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t o = (uint32_t)((s >> 2) * 16384 + (s & 3) * 32) >> 4;
                     const uint32_t ob = (uint32_t)((s >> 2) * 10240 + (s & 3) * 32) >> 4;
-                    mma_bf16(tmem + kTmNum, dPhiQ + o, dSb + ob, kIdRO, 1);
+                    mma_bf16_warp(tmem + kTmNum, dPhiQ + o, dSb + ob, kIdRO, 1);
                 }
 #pragma unroll
                 for (int s = 8; s < 10; ++s)
-                    mma_bf16(tmem + kTmNum, dPhiQ2 + ((s - 8) * 32 >> 4), dSb2 + ((s - 8) * 32 >> 4), kIdRO, 1);
-                mma_commit(bar(B_NUM_FULL));  // also: Phi'_Q buffer free
+                    mma_bf16_warp(tmem + kTmNum, dPhiQ2 + ((s - 8) * 32 >> 4), dSb2 + ((s - 8) * 32 >> 4), kIdRO, 1);
+                mma_commit_warp(bar(B_NUM_FULL));  // also: Phi'_Q buffer free
                 // state update operand Phi'_K(c)
-                if (!(ok = mbar_wait(bar(B_PHK_FULL), pc, abort, status))) break;
-                LA_TR(TR_MMA, c, 3);
+                if (!(ok = wwait(bar(B_PHK_FULL), pc))) break;
+                if (lane == 0) LA_TR(TR_MMA, c, 3);
                 tc_fence_after();
                 // state update: [S'^T ; z'] += [V | 1]^T Phi'_K, 16 tokens per MMA
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_bf16(tmem + kTmS, dV + s * (2048 >> 4), dPhiK + s * (2048 >> 4), kIdUp, 1);
-                mma_commit(bar(B_S_FULL));  // also: Phi'_K and V(c) buffers free (gen forwards the latter)
-                LA_TR(TR_MMA, c, 4);
+                    mma_bf16_warp(tmem + kTmS, dV + s * (2048 >> 4), dPhiK + s * (2048 >> 4), kIdUp, 1);
+                mma_commit_warp(bar(B_S_FULL));  // also: Phi'_K and V(c) buffers free (gen forwards the latter)
+                if (lane == 0) LA_TR(TR_MMA, c, 4);
             }
             // every issued MMA must finish before TMEM is released
-            mma_commit(bar(B_FINAL));
+            __syncwarp();
+            mma_commit_warp(bar(B_FINAL));
             drain_wait(bar(B_FINAL), 0);
         }
 #ifdef LA_TRACE
@@ -436,7 +440,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PHQ_FULL));
+            if (lane == 0) mbar_arrive(bar(B_RO_READY));
             if (tid == 128) LA_TR(TR_GEN, c, 1);
             // past the end or left padding: no contribution to S', z'
             bool pad = c * kC + t >= N;
@@ -517,11 +521,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL));
+            if (lane == 0) mbar_arrive(bar(B_PV_READY));
             if (tid == 256 + 96) LA_TR(TR_EPI, c, 1);
             return true;
         };
-        if (lane == 0) mbar_arrive(bar(B_SB_FULL));  // phase 0: initial operand written in set-up
+        if (lane == 0) mbar_arrive(bar(B_RO_READY));  // phase 0: initial operand written in set-up
         if (do_p(0)) {
             for (int c = 0; c < n; ++c) {
                 if (c + 1 < n && !do_p(c + 1)) break;
@@ -542,7 +546,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     fence_async_smem();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_SB_FULL));
+                    if (lane == 0) mbar_arrive(bar(B_RO_READY));
                 }
             }
         }
@@ -552,7 +556,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int i = 32 * w + lane;          // query row (num lane) / value row d of S'^T
         const bool zrow = (w == 2);           // warp 14: lane 64 holds z'
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
-        if (lane == 0) mbar_arrive(bar(B_SB_FULL));  // phase 0: initial operand written in set-up
+        if (lane == 0) {
+            mbar_arrive(bar(B_RO_READY));  // phase 0: initial operand written in set-up
+            mbar_arrive(bar(B_PV_READY));  // phase 0: num starts drained
+        }
         for (int c = 0; c < n; ++c) {
             // ---- y(c)
             if (!mbar_wait(bar(B_NUM_FULL), (uint32_t)c & 1u, abort, status)) break;
@@ -564,7 +571,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tmem_load64_1_sync(tmem + lanebase + kTmNum, 64, r, dr);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_NUM_EMPTY));
+                if (lane == 0) mbar_arrive(bar(B_PV_READY));  // num of chunk c drained
                 // y rows of this warp -> its 4 KB staging tile -> one bulk tensor store
                 // (rows past N are clipped by the store)
                 float inv = 1.0f / (__uint_as_float(dr) + eps);
@@ -613,7 +620,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_SB_FULL));
+                if (lane == 0) mbar_arrive(bar(B_RO_READY));
             }
             if (tid == 384) LA_TR(TR_CONV, c, 1);
         }
