@@ -418,7 +418,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #endif
     } else if (warp >= 4 && warp < 8) {
         // ================= feature generation (one token per thread) =================
+        // and the conversion of state feature groups 3, 4 after each update
         const int t = tid - 128;
+        const int wq = warp - 4;                        // TMEM lane quarter of this warp
+        const uint32_t lanebase = (uint32_t)(32 * wq) << 16;
+        const bool zrow = (wq == 2);                    // lane 64 holds z'
+        if (lane == 0) mbar_arrive(bar(B_RO_READY));  // phase 0: initial operand written in set-up
         for (int c = 0; c < n; ++c) {
             const int st = c % kStages;
             const uint32_t pc = (uint32_t)c & 1u;
@@ -448,6 +453,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // the update of chunk c - 1 (S_FULL) released the Phi'_K buffer and V(c - 1)
             if (!mbar_wait(bar(B_S_FULL), pc ^ 1u, abort, status)) break;
             if (c > 0 && tid == 128) mbar_arrive(bar(B_V_EMPTY + (c - 1) % kStages));
+            if (c > 0) {
+                // state after chunk c - 1, feature groups 3, 4 -> operand of the read-out of c
+                __syncwarp();
+                tc_fence_after();
+                if (wq < 3)
+                    convert_groups<3, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, 32 * wq + lane, zrow, lane,
+                                                 pow_gamma(chunk_len(c)));
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_RO_READY));
+            }
             if (tid == 128) LA_TR(TR_GEN, c, 2);
             if constexpr (kDecay) {  // token t enters the state after the chunk with gamma^(L-1-t)
                 const float lk = pow_gamma(max(chunk_len(c) - 1 - t, 0));
@@ -525,30 +542,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (tid == 256 + 96) LA_TR(TR_EPI, c, 1);
             return true;
         };
-        if (lane == 0) mbar_arrive(bar(B_RO_READY));  // phase 0: initial operand written in set-up
-        if (do_p(0)) {
-            for (int c = 0; c < n; ++c) {
-                if (c + 1 < n && !do_p(c + 1)) break;
-                // second part of the state conversion: feature groups 3, 4
-                if (!mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status)) break;
-                __syncwarp();
-                tc_fence_after();
-                const bool last = (c == n - 1);
-                if (w < 3) {
-                    if (!last)
-                        convert_groups<3, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane,
-                                                     pow_gamma(chunk_len(c + 1)));
-                    else store_final_groups(tmem + lanebase + kTmS, 3, 2, i, zrow, lane, rows_tab, s0h,
-                                            s_outh, z0h, z_outh, anti_decay);
-                }
-                __syncwarp();
-                if (!last) {
-                    fence_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_RO_READY));
-                }
-            }
+        // Every update phase is observed in order (a parity wait may not skip a
+        // phase), though only the last one is used: the final state, feature
+        // groups 3, 4.  Their per-chunk conversions run in the gen warps, which
+        // keeps this role free for P.
+        bool ok = do_p(0);
+        for (int c = 0; ok && c < n; ++c) {
+            if (c + 1 < n && !(ok = do_p(c + 1))) break;
+            ok = mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status);
+        }
+        if (ok) {
+            __syncwarp();
+            tc_fence_after();
+            if (w < 3)
+                store_final_groups(tmem + lanebase + kTmS, 3, 2, i, zrow, lane, rows_tab, s0h, s_outh, z0h,
+                                   z_outh, anti_decay);
         }
     } else if (warp >= 12) {
         // ========== output epilogue y = num / den, then state conversion ==========
