@@ -12,6 +12,8 @@ times the other two calls of the path, reported under ``legs``:
     twice (2N = 65536 tokens), timed against the prefix call;
   - prefill_decay / decode_decay: the long-prefill and decode workloads with a
     fixed per-head decay 1 - 2^-(4+h) (la_prefill_decay, la_decode_step_decay);
+  - prefill_dk8/24/32: la_prefill on the general feature-dimension path
+    (B=4, H=16, N=4096);
   - decode: la_decode_step on B=128, H=16, 512 consecutive steps captured in
     one CUDA graph, state from a 2048-token prefill (tokens/s and HBM GB/s).
 Inputs are seeded synthetic tensors already resident in HBM and larger than
@@ -396,6 +398,33 @@ def leg_prefill_decay(la, args, dist, dev):
     return {"ms": ms, "B": B, "H": H, "N": N}
 
 
+def leg_general_dk(la, args, dist, dev):
+    """la_prefill on the general feature-dimension path (d' = 8, 24, 32) at
+    B=4, H=16, N=4096, bf16, with an initial state."""
+    out = {}
+    for dk in (8, 24, 32):
+        D = 1 + dk + dk * dk
+        B, H, N = 4, 16, 4096
+        g = torch.Generator(device=dev)
+        g.manual_seed(shard_seed(1500 + dk, dist.rank))
+        q = gen_device((B, H, N, dk), g, dev=dev)
+        k = gen_device((B, H, N, dk), g, dev=dev)
+        v = gen_device((B, H, N, 64), g, dev=dev)
+        s0 = torch.randn((B, H, D, 64), generator=g, device=dev)
+        z0 = torch.rand((B, H, D), generator=g, device=dev) + 64.0
+        y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
+        s = torch.empty_like(s0)
+        z = torch.empty_like(z0)
+
+        def step():
+            la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z)
+
+        ms = time_loop(step, max(1, args.steps // 20), 3, dist)
+        la.check_device_status()
+        out[dk] = {"ms": ms, "B": B, "H": H, "N": N, "D": D}
+    return out
+
+
 def leg_decode(la, args, dist, dev, decay: bool = False):
     """512 decode steps in one CUDA graph (with decay: la_decode_step_decay)."""
     w = inputs.WORKLOADS[5]
@@ -497,7 +526,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--legs", default="prefill,prefix,prefix_padded,jrt_prompt,prefill_decay,decode,decode_decay")
+    ap.add_argument("--legs",
+                    default="prefill,prefix,prefix_padded,jrt_prompt,prefill_decay,general_dk,decode,decode_decay")
     ap.add_argument("--decode-steps", type=int, default=512)
     ap.add_argument("--cpu-sample-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -534,6 +564,8 @@ def main():
         res["jrt_prompt"] = leg_jrt_prompt(la, args, dist, dev)
     if "prefill_decay" in legs:
         res["prefill_decay"] = leg_prefill_decay(la, args, dist, dev)
+    if "general_dk" in legs:
+        res["general_dk"] = leg_general_dk(la, args, dist, dev)
     if "decode" in legs:
         res["decode"] = leg_decode(la, args, dist, dev)
     if "decode_decay" in legs:
@@ -624,6 +656,15 @@ def main():
             "tokens_per_s": W * r["B"] * r["N"] / t, "achieved_tflops": fl / t / 1e12,
             "tc_frac": fl / t / 1e12 / pk["bf16_tflops"]}
         launches += max(1, args.steps // 2)
+    if "general_dk" in res:
+        for dk, r in res["general_dk"].items():
+            t = r["ms"] / 1e3
+            fl = r["B"] * r["H"] * r["N"] * 4 * r["D"] * 65   # readout + update, 2*D*(d_v+1) each
+            line["legs"][f"prefill_dk{dk}"] = {
+                "workload": f"prefill-bf16-B{r['B']}-H{r['H']}-N{r['N']}-dk{dk}-D{r['D']}-s0",
+                "ms_per_call": r["ms"], "tokens_per_s": W * r["B"] * r["N"] / t,
+                "achieved_tflops": fl / t / 1e12, "path": "CUDA cores (general d')"}
+            launches += max(1, args.steps // 20)
     for dname in ("decode", "decode_decay"):
         if dname not in res:
             continue

@@ -23,9 +23,11 @@
  *    word read by la_check_device_status).
  *  - Activations q, k, v, k_e, v_e and the output y have dtype `dtype`
  *    (LA_DTYPE_BF16 or LA_DTYPE_F32).  States s, z are always fp32.
- *    Layouts: q, k [B][H][N][16]; v, y [B][H][N][64]; k_e [B][H][M][16];
- *    v_e [B][H][M][64]; s [B][H][273][64]; z [B][H][273].
- *  - Only d_feat = 16 and d_v = 64 are implemented (LA_ERR_UNSUPPORTED else).
+ *    Layouts: q, k [B][H][N][d_feat]; v, y [B][H][N][64]; k_e [B][H][M][16];
+ *    v_e [B][H][M][64]; s [B][H][D][64]; z [B][H][D] (D = 273 at d_feat = 16).
+ *  - d_v = 64.  d_feat = 16 everywhere; la_prefill and la_decode_step also take
+ *    d_feat = 8, 24, 32 (D = 1 + d_feat + d_feat^2 rows in every state buffer,
+ *    general CUDA-core path).  Anything else is LA_ERR_UNSUPPORTED.
  *  - Every pointer must be 16-byte aligned (LA_ERR_MISALIGNED else).
  *  - s0 / z0 may be NULL, meaning a zero initial state (both or neither).
  *    s_out / z_out may be NULL, meaning "do not write the final state".

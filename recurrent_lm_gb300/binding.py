@@ -18,6 +18,11 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblinattn.so")
 D_FEAT, D_V, D_PHI = 16, 64, 273
 
+
+def feature_dim(dk: int) -> int:
+    """D = 1 + d' + d'^2: rows of the state for feature dimension d'."""
+    return 1 + dk + dk * dk
+
 (LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_MISALIGNED, LA_ERR_CUDA, LA_ERR_TIMEOUT,
  LA_ERR_SCRATCH_TOO_SMALL) = range(7)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
@@ -133,40 +138,41 @@ def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
     [0, 1] (la_prefill_decay), or None; not combined with left_pad.
     Returns (y, s_out, z_out); the states are None when want_state is False."""
     lib = load_library()
-    B, H, N, _ = q.shape
+    B, H, N, dk = q.shape
+    D = feature_dim(dk)
     dt = q.dtype
-    _need(q, "q", (B, H, N, D_FEAT), dt)
-    _need(k, "k", (B, H, N, D_FEAT), dt)
+    _need(q, "q", (B, H, N, dk), dt)
+    _need(k, "k", (B, H, N, dk), dt)
     _need(v, "v", (B, H, N, D_V), dt)
     if s0 is not None or z0 is not None:
-        _need(s0, "s0", (B, H, D_PHI, D_V), torch.float32)
-        _need(z0, "z0", (B, H, D_PHI), torch.float32)
+        _need(s0, "s0", (B, H, D, D_V), torch.float32)
+        _need(z0, "z0", (B, H, D), torch.float32)
     if y is None:
         y = torch.empty((B, H, N, D_V), dtype=dt, device=q.device)
     _need(y, "y", (B, H, N, D_V), dt)
     if want_state:
         if s_out is None:
-            s_out = torch.empty((B, H, D_PHI, D_V), dtype=torch.float32, device=q.device)
+            s_out = torch.empty((B, H, D, D_V), dtype=torch.float32, device=q.device)
         if z_out is None:
-            z_out = torch.empty((B, H, D_PHI), dtype=torch.float32, device=q.device)
+            z_out = torch.empty((B, H, D), dtype=torch.float32, device=q.device)
     if s_out is not None:
-        _need(s_out, "s_out", (B, H, D_PHI, D_V), torch.float32)
+        _need(s_out, "s_out", (B, H, D, D_V), torch.float32)
     if z_out is not None:
-        _need(z_out, "z_out", (B, H, D_PHI), torch.float32)
+        _need(z_out, "z_out", (B, H, D), torch.float32)
     _need_pad(left_pad, B)
     if gamma is not None:
         if left_pad is not None:
             raise ValueError("left_pad and gamma cannot be combined")
         _need(gamma, "gamma", (H,), torch.float32)
         _raise(lib.la_prefill_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(gamma),
-                                    _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q),
+                                    _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, dk, D_V, _dt(q),
                                     float(eps), _stream(stream)))
     elif left_pad is None:
         _raise(lib.la_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
-                              _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q), float(eps), _stream(stream)))
+                              _ptr(z_out), B, H, N, dk, D_V, _dt(q), float(eps), _stream(stream)))
     else:
         _raise(lib.la_prefill_padded(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(left_pad),
-                                     _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q),
+                                     _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, dk, D_V, _dt(q),
                                      float(eps), _stream(stream)))
     return y, s_out, z_out
 
@@ -259,13 +265,14 @@ def decode_step(q, k, v, s, z, *, eps: float = 0.0, y=None, s_out=None, z_out=No
     z [B,H,273] fp32.  With inplace=True the state is updated in s, z.
     gamma: CUDA fp32 [H] per-head decay (la_decode_step_decay), or None."""
     lib = load_library()
-    B, H, _ = q.shape
+    B, H, dk = q.shape
+    D = feature_dim(dk)
     dt = q.dtype
-    _need(q, "q", (B, H, D_FEAT), dt)
-    _need(k, "k", (B, H, D_FEAT), dt)
+    _need(q, "q", (B, H, dk), dt)
+    _need(k, "k", (B, H, dk), dt)
     _need(v, "v", (B, H, D_V), dt)
-    _need(s, "s", (B, H, D_PHI, D_V), torch.float32)
-    _need(z, "z", (B, H, D_PHI), torch.float32)
+    _need(s, "s", (B, H, D, D_V), torch.float32)
+    _need(z, "z", (B, H, D), torch.float32)
     if inplace:
         s_out, z_out = s, z
     if s_out is None:
@@ -276,12 +283,12 @@ def decode_step(q, k, v, s, z, *, eps: float = 0.0, y=None, s_out=None, z_out=No
         y = torch.empty((B, H, D_V), dtype=dt, device=q.device)
     if gamma is None:
         _raise(lib.la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(z), _ptr(s_out),
-                                  _ptr(z_out), _ptr(y), B, H, D_FEAT, D_V, _dt(q), float(eps),
+                                  _ptr(z_out), _ptr(y), B, H, dk, D_V, _dt(q), float(eps),
                                   _stream(stream)))
     else:
         _need(gamma, "gamma", (H,), torch.float32)
         _raise(lib.la_decode_step_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(s), _ptr(z),
-                                        _ptr(s_out), _ptr(z_out), _ptr(y), B, H, D_FEAT, D_V, _dt(q),
+                                        _ptr(s_out), _ptr(z_out), _ptr(y), B, H, dk, D_V, _dt(q),
                                         float(eps), _stream(stream)))
     return y, s_out, z_out
 

@@ -70,7 +70,7 @@ constexpr int64_t kMaxBH = (int64_t(1) << 31) - 1;
 constexpr int64_t kMaxTokens = int64_t(1) << 40;
 
 la_status check_common(int64_t B, int64_t H, int64_t N, int d_feat, int d_v, la_dtype dtype) {
-    if (d_feat != kDFeat || d_v != kDV) return LA_ERR_UNSUPPORTED;
+    if (!la::supported_dk(d_feat) || d_v != kDV) return LA_ERR_UNSUPPORTED;
     if (dtype != LA_DTYPE_F32 && dtype != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
     if (B < 1 || H < 1 || N < 0) return LA_ERR_INVALID_ARG;
     if (B > kMaxBH / H) return LA_ERR_INVALID_ARG;
@@ -99,12 +99,13 @@ PrefixLayout prefix_layout(int64_t BH, int64_t M) {
     return L;
 }
 
-cudaError_t run_prefill(const la::PrefillArgs &a, la_dtype dtype, cudaStream_t st) {
+cudaError_t run_prefill(const la::PrefillArgs &a, la_dtype dtype, cudaStream_t st, int dk = kDFeat) {
     const int64_t BH = a.B * a.H;
     if (a.N == 0) {
         if (!a.s_out && !a.z_out) return cudaSuccess;
-        return la::launch_state_copy(a.s0, a.z0, a.s_out, a.z_out, BH, st);
+        return la::launch_state_copy(la::feat_dim(dk), a.s0, a.z0, a.s_out, a.z_out, BH, st);
     }
+    if (dk != kDFeat) return la::launch_prefill_general(a, dk, dtype, st);
     if (dtype == LA_DTYPE_BF16) return la::launch_prefill_tc(a, st);
     return la::launch_prefill_simt(a, dtype, st);
 }
@@ -121,7 +122,9 @@ const char *la_status_string(la_status s) {
     switch (s) {
         case LA_OK: return "ok";
         case LA_ERR_INVALID_ARG: return "invalid argument (shape, NULL pointer, M > N or overlapping buffers)";
-        case LA_ERR_UNSUPPORTED: return "unsupported (d_feat must be 16, d_v 64, dtype f32/bf16, device sm_103)";
+        case LA_ERR_UNSUPPORTED:
+            return "unsupported (d_feat 8/16/24/32 (padding, decay and prefix: 16 only), d_v 64, dtype f32/bf16, "
+                   "device sm_103)";
         case LA_ERR_MISALIGNED: return "a buffer is not 16-byte aligned";
         case LA_ERR_CUDA: return "CUDA runtime error or kernel launch failure";
         case LA_ERR_TIMEOUT: return "a bounded device-side wait gave up";
@@ -143,6 +146,9 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
                        la_dtype dtype, float eps, la_stream_t stream, const float *gamma = nullptr) {
     la_status st = check_common(B, H, N, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
+    // padding and decay exist for d' = 16 only
+    if ((left_pad || gamma) && d_feat != kDFeat) return LA_ERR_UNSUPPORTED;
+    const int64_t D = la::feat_dim(d_feat);
     if ((s0 == nullptr) != (z0 == nullptr)) return LA_ERR_INVALID_ARG;
     if (N > 0 && (!q || !k || !v || !y)) return LA_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, s0, z0, y, s_out, z_out};
@@ -150,11 +156,11 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
         if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
     const int64_t BH = B * H;
     const size_t es = esize(dtype);
-    const Range in[] = {{q, es * BH * N * kDFeat}, {k, es * BH * N * kDFeat},
-                        {v, es * BH * N * kDV}, {s0, sizeof(float) * BH * kD * kDV},
-                        {z0, sizeof(float) * BH * kD}};
-    const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * kD * kDV},
-                         {z_out, sizeof(float) * BH * kD}};
+    const Range in[] = {{q, es * BH * N * d_feat}, {k, es * BH * N * d_feat},
+                        {v, es * BH * N * kDV}, {s0, sizeof(float) * BH * D * kDV},
+                        {z0, sizeof(float) * BH * D}};
+    const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * D * kDV},
+                         {z_out, sizeof(float) * BH * D}};
     if (any_overlap(in, 5, out, 3)) return LA_ERR_INVALID_ARG;
     if ((left_pad && !aligned4(left_pad)) || (gamma && !aligned4(gamma))) return LA_ERR_MISALIGNED;
     for (const Range &o : out)
@@ -164,7 +170,7 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
     unsigned *status;
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
     la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad, gamma};
-    return to_status(run_prefill(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
+    return to_status(run_prefill(a, dtype, reinterpret_cast<cudaStream_t>(stream), d_feat));
 }
 
 la_status prefix_impl(const void *q, const void *k, const void *v, const void *k_e,
@@ -175,6 +181,7 @@ la_status prefix_impl(const void *q, const void *k, const void *v, const void *k
                       la_stream_t stream) {
     la_status st = check_common(B, H, N, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
+    if (d_feat != kDFeat) return LA_ERR_UNSUPPORTED;  // the prefix path exists for d' = 16
     if (M < 0 || M > N) return LA_ERR_INVALID_ARG;
     if (M == 0)
         return prefill_impl(q, k, v, s0, z0, left_pad, y, s_out, z_out, B, H, N, d_feat, d_v,
@@ -284,15 +291,17 @@ la_status decode_impl(const void *q, const void *k, const void *v, const float *
                       la_stream_t stream) {
     la_status st = check_common(B, H, 1, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
+    if (gamma && d_feat != kDFeat) return LA_ERR_UNSUPPORTED;  // decay exists for d' = 16 only
+    const int64_t D = la::feat_dim(d_feat);
     if (!q || !k || !v || !s_in || !z_in || !s_out || !z_out || !y) return LA_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, s_in, z_in, s_out, z_out, y};
     for (const void *p : ptrs)
         if (!aligned16(p)) return LA_ERR_MISALIGNED;
     const int64_t BH = B * H;
     const size_t es = esize(dtype);
-    const size_t sb = sizeof(float) * BH * kD * kDV, zb = sizeof(float) * BH * kD;
+    const size_t sb = sizeof(float) * BH * D * kDV, zb = sizeof(float) * BH * D;
     // exact aliasing s_out == s_in / z_out == z_in is the in-place update
-    const Range in[] = {{q, es * BH * kDFeat}, {k, es * BH * kDFeat}, {v, es * BH * kDV},
+    const Range in[] = {{q, es * BH * d_feat}, {k, es * BH * d_feat}, {v, es * BH * kDV},
                         {s_out == s_in ? nullptr : s_in, sb},
                         {z_out == z_in ? nullptr : z_in, zb}};
     const Range out[] = {{y, es * BH * kDV}, {s_out, sb}, {z_out, zb}};
@@ -309,6 +318,8 @@ la_status decode_impl(const void *q, const void *k, const void *v, const float *
     unsigned *status;
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
     la::DecodeArgs a{q, k, v, s_in, z_in, s_out, z_out, y, B, H, eps, gamma, status};
+    if (d_feat != kDFeat)
+        return to_status(la::launch_decode_general(a, d_feat, dtype, reinterpret_cast<cudaStream_t>(stream)));
     return to_status(la::launch_decode(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 

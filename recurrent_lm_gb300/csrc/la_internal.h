@@ -74,13 +74,20 @@ struct PrefixArgs {
 constexpr int64_t kPrefixSeg = 2048;
 inline int64_t prefix_nseg(int64_t M) { return (M + kPrefixSeg - 1) / kPrefixSeg; }
 
+// Feature dimensions d' with a kernel: 16 (tensor-core and CUDA-core paths)
+// and 8, 24, 32 (the general CUDA-core path).  D = 1 + d' + d'^2.
+inline bool supported_dk(int dk) { return dk == 8 || dk == 16 || dk == 24 || dk == 32; }
+inline int64_t feat_dim(int dk) { return 1 + (int64_t)dk + (int64_t)dk * dk; }
+cudaError_t launch_prefill_general(const PrefillArgs &a, int dk, la_dtype dt, cudaStream_t st);
+cudaError_t launch_decode_general(const DecodeArgs &a, int dk, la_dtype dt, cudaStream_t st);
+
 cudaError_t launch_decode(const DecodeArgs &a, la_dtype dt, cudaStream_t st);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, la_dtype dt, cudaStream_t st);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st);
 cudaError_t launch_prefix_partials_simt(const PrefixArgs &a, la_dtype dt, cudaStream_t st);
 cudaError_t launch_prefix_partials_tc(const PrefixArgs &a, cudaStream_t st);
 cudaError_t launch_prefix_reduce(const PrefixArgs &a, cudaStream_t st);
-cudaError_t launch_state_copy(const float *s0, const float *z0, float *s_out,
+cudaError_t launch_state_copy(int64_t D, const float *s0, const float *z0, float *s_out,
                               float *z_out, int64_t BH, cudaStream_t st);
 
 }  // namespace la

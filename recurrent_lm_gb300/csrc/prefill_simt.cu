@@ -210,8 +210,8 @@ __global__ void prefix_reduce_kernel(const float *__restrict__ part_s,
 
 __global__ void state_copy_kernel(const float *__restrict__ s0,
                                   const float *__restrict__ z0, float *s_out,
-                                  float *z_out, int64_t BH) {
-    const int64_t ns = BH * kD * kDV, nz = BH * kD;
+                                  float *z_out, int64_t BH, int64_t D) {
+    const int64_t ns = BH * D * kDV, nz = BH * D;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < ns + nz;
          e += (int64_t)gridDim.x * blockDim.x) {
         if (e < ns) {
@@ -266,10 +266,10 @@ cudaError_t launch_prefix_reduce(const PrefixArgs &a, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_state_copy(const float *s0, const float *z0, float *s_out,
+cudaError_t launch_state_copy(int64_t D, const float *s0, const float *z0, float *s_out,
                               float *z_out, int64_t BH, cudaStream_t st) {
-    const int64_t total = BH * ((int64_t)kD * kDV + kD);
-    state_copy_kernel<<<grid_for(total, 256), 256, 0, st>>>(s0, z0, s_out, z_out, BH);
+    const int64_t total = BH * (D * kDV + D);
+    state_copy_kernel<<<grid_for(total, 256), 256, 0, st>>>(s0, z0, s_out, z_out, BH, D);
     return cudaGetLastError();
 }
 

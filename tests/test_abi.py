@@ -65,7 +65,8 @@ def call_prefill(lib, B=1, H=1, N=8, dk=16, dv=64, dtype=1, ptrs=None, s0=True):
 
 
 def test_prefill_rejects_unsupported_dims(lib):
-    assert call_prefill(lib, dk=8) == binding.LA_ERR_UNSUPPORTED
+    assert call_prefill(lib, dk=12) == binding.LA_ERR_UNSUPPORTED  # d' in {8, 16, 24, 32} only
+    assert call_prefill(lib, dk=64) == binding.LA_ERR_UNSUPPORTED
     assert call_prefill(lib, dv=32) == binding.LA_ERR_UNSUPPORTED
     assert call_prefill(lib, dtype=7) == binding.LA_ERR_UNSUPPORTED
 
@@ -177,3 +178,18 @@ def test_padded_calls_reject_null_misaligned_or_overlapping_pads(lib):
                                         1 << 30, *pargs) == binding.LA_ERR_MISALIGNED
     assert lib.la_prefix_prefill_padded(q, k, v, ke, ve, 9, s0, z0, fake(9), y, so, zo, ws, 1 << 30,
                                         *pargs) == binding.LA_ERR_INVALID_ARG  # M > N
+
+
+def test_padding_decay_and_prefix_need_d16(lib):
+    """The general-d' path covers la_prefill and la_decode_step; the padded,
+    decayed and prefix calls exist for d' = 16 only."""
+    p = [fake(i) for i in range(8)]
+    q, k, v, s0, z0, y, so, zo = p
+    assert lib.la_prefill_padded(q, k, v, s0, z0, fake(9), y, so, zo, 1, 1, 8, 8, 64, 1, 0.0,
+                                 None) == binding.LA_ERR_UNSUPPORTED
+    assert lib.la_prefill_decay(q, k, v, s0, z0, fake(9), y, so, zo, 1, 1, 8, 24, 64, 1, 0.0,
+                                None) == binding.LA_ERR_UNSUPPORTED
+    assert lib.la_prefix_prefill(q, k, v, fake(10), fake(11), 4, s0, z0, y, so, zo, fake(12), 1 << 30,
+                                 1, 1, 8, 32, 64, 1, 0.0, None) == binding.LA_ERR_UNSUPPORTED
+    assert lib.la_decode_step_decay(q, k, v, fake(9), s0, z0, so, zo, y, 1, 1, 8, 64, 1, 0.0,
+                                    None) == binding.LA_ERR_UNSUPPORTED

@@ -1,0 +1,60 @@
+"""GPU parity of the general feature-dimension path (d' in {8, 24, 32}, D =
+1 + d' + d'^2) of la_prefill and la_decode_step against the fp64 oracle, which
+implements the same map for any d' (BASED notes, sec. 2.3)."""
+import pytest
+import torch
+
+import oracle
+import recurrent_lm_gb300 as la
+from recurrent_lm_gb300 import inputs
+from helpers import TOL, assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def check(got, ref, tol, what=""):
+    for name, a, r in zip("ysz", got, ref):
+        assert_close(name + what, a, r, tol)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dk", [8, 24, 32])
+@pytest.mark.parametrize("N", [1, 37, 300])
+def test_general_dk_prefill(dtype, dk, N):
+    D = oracle.feature_dim(dk)
+    q, k, v, _, _ = inputs.qkv(2, 3, N, seed=1200 + dk + N, dtype=dtype, dk=dk)
+    s0, z0 = inputs.random_state(2, 3, seed=1201 + dk, D=D)
+    got = la.prefill(q.to(DEV), k.to(DEV), v.to(DEV), s0.to(DEV), z0.to(DEV))
+    torch.cuda.synchronize()
+    ref = oracle.prefill(q, k, v, s0, z0)
+    check(got, ref, TOL[dtype], f" dk={dk} N={N}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("dk", [8, 24, 32])
+def test_general_dk_decode_in_place_equals_prefill(dtype, dk):
+    """n decode steps in place (the state buffers are also the outputs) equal
+    the oracle's prefill of those n tokens from the same initial state."""
+    D, n = oracle.feature_dim(dk), 9
+    q, k, v, _, _ = inputs.qkv(2, 2, n, seed=1300 + dk, dtype=dtype, dk=dk)
+    s0, z0 = inputs.random_state(2, 2, seed=1301 + dk, D=D)
+    s, z = s0.to(DEV), z0.to(DEV)
+    ys = []
+    for i in range(n):
+        y, _, _ = la.decode_step(q[:, :, i].contiguous().to(DEV), k[:, :, i].contiguous().to(DEV),
+                                 v[:, :, i].contiguous().to(DEV), s, z, inplace=True)
+        ys.append(y)
+    torch.cuda.synchronize()
+    yr, sr, zr = oracle.prefill(q, k, v, s0, z0)
+    check((torch.stack(ys, dim=2), s, z), (yr, sr, zr), TOL[dtype], f" dk={dk}")
+
+
+def test_general_dk_zero_length_copies_state():
+    D = oracle.feature_dim(24)
+    s0, z0 = inputs.random_state(1, 2, seed=1400, D=D)
+    e = torch.empty((1, 2, 0, 24), device=DEV)
+    ev = torch.empty((1, 2, 0, 64), device=DEV)
+    _, s, z = la.prefill(e, e, ev, s0.to(DEV), z0.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(s.cpu(), s0) and torch.equal(z.cpu(), z0)
