@@ -262,17 +262,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     // the antisymmetric part of s0 bypasses the compact state: it decays by gamma^N
     const float anti_decay = kDecay ? powf(pow_gamma(1), (float)N) : 1.f;
 
-    // initial state, before any role starts: S'^T rows (values d = 0..63, lanes of
-    // warps 12, 13) and z' (lanes 64.., warp 14) in TMEM, and their bf16 operand rows
-    if (warp >= 12 && warp < 15) {
-        const int w = warp - 12;
+    // initial state, before any role starts: S'^T rows (values d = 0..63, TMEM lane
+    // quarters 0, 1) and z' (lane 64, quarter 2) in TMEM, and their bf16 operand
+    // rows.  The 5 feature groups of each quarter are spread over the quarter's 4
+    // warps (warp % 4 selects the quarter) so that their loads are in flight together.
+    if ((warp & 3) < 3) {
+        const int w = warp & 3;
         const int d = 32 * w + lane;
         const bool zrow = (w == 2);
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
         const float *col0 = zrow ? z0h : (s0h ? s0h + d : nullptr);
         const int stride = zrow ? 1 : kDV;
 #pragma unroll 1
-        for (int g = 0; g < kNFeat / 32; ++g) {
+        for (int g = warp >> 2; g < kNFeat / 32; g += 4) {
             uint32_t r[32];
             compact_initial_group(col0, stride, rows_tab + 32 * g, r);
             __syncwarp();
@@ -424,6 +426,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const uint32_t lanebase = (uint32_t)(32 * wq) << 16;
         const bool zrow = (wq == 2);                    // lane 64 holds z'
         if (lane == 0) mbar_arrive(bar(B_RO_READY));  // phase 0: initial operand written in set-up
+        bool gen_done = false;
         for (int c = 0; c < n; ++c) {
             const int st = c % kStages;
             const uint32_t pc = (uint32_t)c & 1u;
@@ -477,6 +480,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PHK_FULL));
             if (tid == 128) LA_TR(TR_GEN, c, 3);
+            if (c == n - 1) gen_done = true;
+        }
+        // final state, feature groups 3, 4, once the last update completed (the
+        // loop observed every earlier update phase in order)
+        if (gen_done && mbar_wait(bar(B_S_FULL), (uint32_t)(n - 1) & 1u, abort, status)) {
+            __syncwarp();
+            tc_fence_after();
+            if (wq < 3)
+                store_final_groups(tmem + lanebase + kTmS, 3, 2, 32 * wq + lane, zrow, lane, rows_tab, s0h, s_outh,
+                                   z0h, z_outh, anti_decay);
         }
     } else if (warp >= 8 && warp < 12) {
         // ================= P epilogue: P = 1 + T/4 + T^2/32, causal, in place =================
@@ -544,8 +557,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         };
         // Every update phase is observed in order (a parity wait may not skip a
         // phase), though only the last one is used: the final state, feature
-        // groups 3, 4.  Their per-chunk conversions run in the gen warps, which
-        // keeps this role free for P.
+        // groups 1, 2.  The per-chunk conversions of groups 3, 4 run in the gen
+        // warps, which keeps this role free for P.
         bool ok = do_p(0);
         for (int c = 0; ok && c < n; ++c) {
             if (c + 1 < n && !(ok = do_p(c + 1))) break;
@@ -554,8 +567,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         if (ok) {
             __syncwarp();
             tc_fence_after();
-            if (w < 3)
-                store_final_groups(tmem + lanebase + kTmS, 3, 2, i, zrow, lane, rows_tab, s0h, s_outh, z0h,
+            if (w < 3)  // final state, feature groups 1, 2
+                store_final_groups(tmem + lanebase + kTmS, 1, 2, i, zrow, lane, rows_tab, s0h, s_outh, z0h,
                                    z_outh, anti_decay);
         }
     } else if (warp >= 12) {
@@ -619,7 +632,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     __syncwarp();
                     convert_groups<2, 1, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                 } else {
-                    store_final_groups(tmem + lanebase + kTmS, 0, 3, i, zrow, lane, rows_tab, s0h, s_outh,
+                    // final state, feature group 0 (groups 1..4: P and gen warps)
+                    store_final_groups(tmem + lanebase + kTmS, 0, 1, i, zrow, lane, rows_tab, s0h, s_outh,
                                        z0h, z_outh, anti_decay);
                 }
                 __syncwarp();
