@@ -555,32 +555,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (tid == 256 + 96) LA_TR(TR_EPI, c, 1);
             return true;
         };
-        // Every update phase is observed in order (a parity wait may not skip a
-        // phase), though only the last one is used: the final state, feature
-        // groups 1, 2.  The per-chunk conversions of groups 3, 4 run in the gen
-        // warps, which keeps this role free for P.
+        // After P(c + 1) (done well before the update of chunk c completes), the
+        // state after chunk c, feature groups 0..2: the operand of the read-out of
+        // chunk c + 1, or the final state (groups 3, 4: gen warps).
+        if (lane == 0) mbar_arrive(bar(B_RO_READY));  // phase 0: initial operand written in set-up
         bool ok = do_p(0);
         for (int c = 0; ok && c < n; ++c) {
             if (c + 1 < n && !(ok = do_p(c + 1))) break;
-            ok = mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status);
-        }
-        if (ok) {
+            if (!(ok = mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status))) break;
             __syncwarp();
             tc_fence_after();
-            if (w < 3)  // final state, feature groups 1, 2
-                store_final_groups(tmem + lanebase + kTmS, 1, 2, i, zrow, lane, rows_tab, s0h, s_outh, z0h,
-                                   z_outh, anti_decay);
+            const bool last = (c == n - 1);
+            if (w < 3) {
+                if (!last) {
+                    const float dn = pow_gamma(chunk_len(c + 1));
+                    convert_groups<0, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
+                    __syncwarp();
+                    convert_groups<2, 1, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
+                } else {
+                    store_final_groups(tmem + lanebase + kTmS, 0, 3, i, zrow, lane, rows_tab, s0h, s_outh, z0h,
+                                       z_outh, anti_decay);
+                }
+                __syncwarp();
+            }
+            if (!last) {
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_RO_READY));
+            }
         }
     } else if (warp >= 12) {
-        // ========== output epilogue y = num / den, then state conversion ==========
+        // ========== output epilogue y = num / den ==========
         const int w = warp - 12;
         const int i = 32 * w + lane;          // query row (num lane) / value row d of S'^T
         const bool zrow = (w == 2);           // warp 14: lane 64 holds z'
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
-        if (lane == 0) {
-            mbar_arrive(bar(B_RO_READY));  // phase 0: initial operand written in set-up
-            mbar_arrive(bar(B_PV_READY));  // phase 0: num starts drained
-        }
+        if (lane == 0) mbar_arrive(bar(B_PV_READY));  // phase 0: num starts drained
         for (int c = 0; c < n; ++c) {
             // ---- y(c)
             if (!mbar_wait(bar(B_NUM_FULL), (uint32_t)c & 1u, abort, status)) break;
@@ -619,32 +630,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
             }
             if (tid == 384) LA_TR(TR_EPI, c, 3);
-            // ---- state after chunk c: bf16 operand for the next read-out, or the final state
-            if (!mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status)) break;
-            if (tid == 384) LA_TR(TR_CONV, c, 0);
-            __syncwarp();
-            tc_fence_after();
-            const bool last = (c == n - 1);
-            if (w < 3) {
-                if (!last) {
-                    const float dn = pow_gamma(chunk_len(c + 1));
-                    convert_groups<0, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
-                    __syncwarp();
-                    convert_groups<2, 1, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
-                } else {
-                    // final state, feature group 0 (groups 1..4: P and gen warps)
-                    store_final_groups(tmem + lanebase + kTmS, 0, 1, i, zrow, lane, rows_tab, s0h, s_outh,
-                                       z0h, z_outh, anti_decay);
-                }
-                __syncwarp();
-            }
-            if (!last) {
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_RO_READY));
-            }
-            if (tid == 384) LA_TR(TR_CONV, c, 1);
         }
         if (lane == 0) bulk_wait0();  // y stores complete before the CTA exits
     }
