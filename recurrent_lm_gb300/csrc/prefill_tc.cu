@@ -361,8 +361,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 // P(c) is in T[b]; V(c) is in; num was drained for chunk c - 1 (which
                 // also means P V of chunk c - 1 completed: the read-out commit covers
                 // every earlier MMA, so T[b ^ 1] may take Q K^T(c + 1)); q, k of c + 1
-                ok = wwait(bar(B_PV_READY), pc) && wwait(bar(B_V_FULL + vs), (uint32_t)(c / kStages) & 1u) &&
-                     (c + 1 >= n || wwait(bar(B_QK_FULL + (c + 1) % kStages), (uint32_t)((c + 1) / kStages) & 1u));
+                // (PV_READY(c) also covers V(c) and q, k of chunk c + 1: a y warp
+                // observes those loads before it arrives, sparing this thread the waits)
+                ok = wwait(bar(B_PV_READY), pc);
                 if (!ok) break;
                 if (lane == 0) LA_TR(TR_MMA, c, 0);
                 tc_fence_after();
@@ -591,8 +592,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int i = 32 * w + lane;          // query row (num lane) / value row d of S'^T
         const bool zrow = (w == 2);           // warp 14: lane 64 holds z'
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
-        if (lane == 0) mbar_arrive(bar(B_PV_READY));  // phase 0: num starts drained
-        for (int c = 0; c < n; ++c) {
+        // PV_READY(c) from the y warps: num drained after chunk c - 1, and (one
+        // lane) the loads P V(c) and Q K^T(c + 1) read, observed in order
+        auto pv_ready = [&](int c) -> bool {
+            if (tid == 384 && c < n &&
+                (!mbar_wait(bar(B_V_FULL + c % kStages), (uint32_t)(c / kStages) & 1u, abort, status) ||
+                 (c + 1 < n && !mbar_wait(bar(B_QK_FULL + (c + 1) % kStages), (uint32_t)((c + 1) / kStages) & 1u,
+                                          abort, status))))
+                return false;
+            if (lane == 0) mbar_arrive(bar(B_PV_READY));
+            return true;
+        };
+        bool ok = pv_ready(0);  // phase 0: num starts drained
+        for (int c = 0; ok && c < n; ++c) {
             // ---- y(c)
             if (!mbar_wait(bar(B_NUM_FULL), (uint32_t)c & 1u, abort, status)) break;
             if (tid == 384) LA_TR(TR_EPI, c, 2);
@@ -603,7 +615,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tmem_load64_1_sync(tmem + lanebase + kTmNum, 64, r, dr);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_PV_READY));  // num of chunk c drained
+                ok = pv_ready(c + 1);  // num of chunk c drained
                 // y rows of this warp -> its 4 KB staging tile -> one bulk tensor store
                 // (rows past N are clipped by the store)
                 float inv = 1.0f / (__uint_as_float(dr) + eps);
