@@ -514,20 +514,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             for (int pp = 0; pp < 2; ++pp) {
                 uint32_t pw[32];
                 if (2 * pp <= w) {
-                    uint32_t r[64];
-                    tmem_load64_sync(tb + 64 * pp, r);
                     const uint64_t c32 = f2pack(0.03125f, 0.03125f), c4 = f2pack(0.25f, 0.25f),
                                    c1 = f2pack(1.0f, 1.0f);
                     const bool diag = 64 * pp + 63 >= 32 * w;  // this block reaches the diagonal
+                    if constexpr (kDecay) {
+                        // in halves of 32 columns: the decay factors (gamma^(i-j), gamma^(i-j-1))
+                        // from the power table need registers too; j > i is masked below
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t r[32];
+                            tmem_load32_sync(tb + 64 * pp + 32 * h, r);
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int key = 64 * pp + 32 * h + 2 * j;
+                                const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
+                                const uint64_t f2 = ld_shared_u64(sb + kSmPow + 8u * (uint32_t)max(i - key, 0));
+                                const uint64_t p2 = fmul2(ffma2(t2, ffma2(t2, c32, c4), c1), f2);
+                                float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
+                                if (diag) {
+                                    if (key > i) p0 = 0.f;
+                                    if (key + 1 > i) p1 = 0.f;
+                                }
+                                pw[16 * h + j] = pack_bf16(p0, p1);
+                            }
+                        }
+                    } else {
+                    uint32_t r[64];
+                    tmem_load64_sync(tb + 64 * pp, r);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
                         uint64_t p2 = ffma2(t2, ffma2(t2, c32, c4), c1);
-                        if constexpr (kDecay) {  // times (gamma^(i-j), gamma^(i-j-1)); j > i is masked below
-                            const int dd = max(i - (64 * pp + 2 * j), 0);
-                            const float2 f = reinterpret_cast<const float2 *>(smem + kSmPow)[dd];
-                            p2 = fmul2(p2, f2pack(f.x, f.y));
-                        }
                         float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
                         if (diag) {
                             const int key = 64 * pp + 2 * j;
@@ -535,6 +552,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                             if (key + 1 > i) p1 = 0.f;
                         }
                         pw[j] = pack_bf16(p0, p1);
+                    }
                     }
                     if (kPad && kmin > 64 * pp) {  // chunk holds left padding: drop padded keys
 #pragma unroll
