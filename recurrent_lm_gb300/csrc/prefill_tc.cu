@@ -34,6 +34,7 @@
 //    the state conversion (TMEM fp32 -> bf16 operand, final state store).
 //  * Every wait is bounded: after ~1 s the kernel records a timeout in the
 //    device status word and every role unwinds.
+#include <type_traits>
 #include <utility>
 
 #include "la_internal.h"
@@ -66,8 +67,7 @@ constexpr uint32_t kSmOnes = 165888;   // [128][64] bf16 ones (the extra rows/co
 constexpr uint32_t kSmQ = 182272;      // 3 x [128][16] bf16 SW32
 constexpr uint32_t kSmK = 194560;      // 3 x [128][16] bf16 SW32
 constexpr uint32_t kSmY = 206848;      // 4 x [32 rows][64] bf16 SW128: y staging for TMA stores
-constexpr uint32_t kSmRows = kSmY + 16384;  // [160] x int4 feature -> ABI row table
-constexpr uint32_t kSmBar = kSmRows + 160 * 16;
+constexpr uint32_t kSmBar = kSmY + 16384;
 constexpr uint32_t kSmPow = kSmBar + 512;  // decay: [129] float2 (gamma^d, gamma^(d-1))
 constexpr uint32_t kSmTotal = kSmPow + 1280;
 constexpr uint32_t kSmAlloc = kSmTotal + 1024;
@@ -83,6 +83,7 @@ enum {
     // waits are expensive after MMA issue.
     B_PV_READY = 14, B_RO_READY, B_PHK_FULL,
     B_NUM_FULL, B_S_FULL, B_FINAL,
+    B_STAGED,   // the final state's value rows are in the shared-memory image
     B_COUNT
 };
 constexpr uint32_t kSmTmemSlot = kSmBar + 8 * B_COUNT;
@@ -149,10 +150,82 @@ __device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, i
     }
 }
 
+// P = 1 + T/4 + T^2/32 for the keys 64 pp .. 64 pp + 63 of query row i (TMEM
+// lane quarter w), with the causal mask (key > i), left padding (key < kmin)
+// and, with decay, the factor gamma^(i - key) from the power table at `pow`.
+// Reads T at `tsrc` + 64 pp and writes the 32 packed bf16 columns to `tdst`,
+// which lie inside the columns this warp has just read.  Rows that see no key
+// of the block (2 pp > w) store zeros.
+template <bool kPad, bool kDecay>
+__device__ __forceinline__ void p_block(uint32_t tsrc, uint32_t tdst, int pp, int i, int w, int kmin,
+                                        uint32_t pow) {
+    uint32_t pw[32];
+    if (2 * pp <= w) {
+        const uint64_t c32 = f2pack(0.03125f, 0.03125f), c4 = f2pack(0.25f, 0.25f), c1 = f2pack(1.0f, 1.0f);
+        const bool diag = 64 * pp + 63 >= 32 * w;  // this block reaches the diagonal
+        if constexpr (kDecay) {
+            // in halves of 32 columns: the decay factors (gamma^(i-j), gamma^(i-j-1))
+            // from the power table need registers too; j > i is masked below
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32];
+                tmem_load32_sync(tsrc + 64 * pp + 32 * h, r);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int key = 64 * pp + 32 * h + 2 * j;
+                    const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
+                    const uint64_t f2 = ld_shared_u64(pow + 8u * (uint32_t)max(i - key, 0));
+                    const uint64_t p2 = fmul2(ffma2(t2, ffma2(t2, c32, c4), c1), f2);
+                    float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
+                    if (diag) {
+                        if (key > i) p0 = 0.f;
+                        if (key + 1 > i) p1 = 0.f;
+                    }
+                    pw[16 * h + j] = pack_bf16(p0, p1);
+                }
+            }
+        } else {
+            uint32_t r[64];
+            tmem_load64_sync(tsrc + 64 * pp, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
+                const uint64_t p2 = ffma2(t2, ffma2(t2, c32, c4), c1);
+                float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
+                if (diag) {
+                    const int key = 64 * pp + 2 * j;
+                    if (key > i) p0 = 0.f;
+                    if (key + 1 > i) p1 = 0.f;
+                }
+                pw[j] = pack_bf16(p0, p1);
+            }
+        }
+        if (kPad && kmin > 64 * pp) {  // chunk holds left padding: drop padded keys
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int key = 64 * pp + 2 * j;
+                if (key + 1 < kmin) pw[j] = 0u;
+                else if (key < kmin) pw[j] &= 0xFFFF0000u;  // low half = the even key
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pw[j] = 0u;
+    }
+    tmem_store32_sync(tdst, pw);
+}
+
+// Image of one head's final [273][64] fp32 state in shared memory, written
+// out with a single bulk copy once the last update has completed (the
+// feature-operand buffers it overlays are free by then).
+constexpr uint32_t kSmStage = kSmPhiQ;
+constexpr uint32_t kStageBytes = (uint32_t)kD * kDV * 4;
+static_assert(kSmStage + kStageBytes <= kSmSb, "final state image overlays Phi'_Q and Phi'_K only");
+
 // Optional per-role timeline of CTA 0 (compile with -DLA_TRACE): SM clock
 // offsets from kernel entry for events of each role and chunk.
-constexpr int kTraceChunks = 512;
 #ifdef LA_TRACE
+constexpr int kTraceChunks = 512;
 __device__ uint32_t g_trace[5][kTraceChunks][8];
 #define LA_TR(role, c, ev)                                                         \
     do {                                                                           \
@@ -186,7 +259,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const uint32_t sb = smem_u32(smem);
     auto bar = [&](int i) { return sb + kSmBar + 8u * (uint32_t)i; };
     volatile int *abort = reinterpret_cast<volatile int *>(smem + kSmAbort);
-    const int4 *rows_tab = reinterpret_cast<const int4 *>(smem + kSmRows);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t bh = blockIdx.x;
@@ -213,12 +285,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_T_FULL + i), 1);
         }
-        mbar_init(bar(B_PV_READY), 4 + 4);
+        mbar_init(bar(B_PV_READY), 6 + 4);  // P warps 8..11, 2, 3; y warps
         mbar_init(bar(B_RO_READY), 4 + 8);
         mbar_init(bar(B_PHK_FULL), 4);
         mbar_init(bar(B_NUM_FULL), 1);
         mbar_init(bar(B_S_FULL), 1);
         mbar_init(bar(B_FINAL), 1);
+        mbar_init(bar(B_STAGED), 4 + 4);  // P and gen warps
         *abort = 0;
         mbar_init_fence();
     }
@@ -232,10 +305,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     for (int i = tid; i < 15 * 20; i += kThreads) {
         const int d = 65 + i / 20, j = i % 20;
         st_shared_v4(sb + kSmSb + sb_chunk_off(d, j), 0u, 0u, 0u, 0u);
-    }
-    if (tid < kNFeat) {
-        const Rows r = abi_rows(tid);
-        reinterpret_cast<int4 *>(smem + kSmRows)[tid] = make_int4(r.r1, r.r2, r.kind, 0);
     }
     fence_async_smem();
     tc_fence_before();
@@ -272,19 +341,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const bool zrow = (w == 2);
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
         const float *col0 = zrow ? z0h : (s0h ? s0h + d : nullptr);
-        const int stride = zrow ? 1 : kDV;
-#pragma unroll 1
-        for (int g = warp >> 2; g < kNFeat / 32; g += 4) {
+        const int64_t stride = zrow ? 1 : kDV;
+        auto load_group = [&](auto gc) {
+            constexpr int G = decltype(gc)::value;
             uint32_t r[32];
-            compact_initial_group(col0, stride, rows_tab + 32 * g, r);
+            compact_initial_group<G>(col0, stride, r, std::make_integer_sequence<int, 32>{});
             __syncwarp();
-            if (!zrow || lane == 0) write_sb_group(sb + kSmSb, zrow ? 64 : d, g, r);
+            if (!zrow || lane == 0) write_sb_group(sb + kSmSb, zrow ? 64 : d, G, r);
             if constexpr (kDecay) {  // the first update starts from gamma^L0 s0
                 const float d0 = pow_gamma(chunk_len(0));
 #pragma unroll
                 for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * d0);
             }
-            tmem_store32_sync(tmem + lanebase + kTmS + 32 * g, r);
+            tmem_store32_sync(tmem + lanebase + kTmS + 32 * G, r);
+        };
+        switch (warp >> 2) {  // warps 0..2 take groups 0 and 4
+            case 0:
+                load_group(std::integral_constant<int, 0>{});
+                load_group(std::integral_constant<int, 4>{});
+                break;
+            case 1: load_group(std::integral_constant<int, 1>{}); break;
+            case 2: load_group(std::integral_constant<int, 2>{}); break;
+            default: load_group(std::integral_constant<int, 3>{}); break;
         }
         fence_async_smem();
         tc_fence_before();
@@ -371,8 +449,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (lane == 0) LA_TR(TR_MMA, c, 1);
                 // intra-chunk: [num | den] = P [V | 1], P from TMEM
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_bf16_ts_warp(tmem + kTmNum, tmem + tm_t(b) + 8 * s, dV + s * (2048 >> 4), kIdPV, s > 0);
+                for (int s = 0; s < 8; ++s)  // keys 16 s..: packed columns 8 s (s < 4), 64 + 8 s (s >= 4)
+                    mma_bf16_ts_warp(tmem + kTmNum, tmem + tm_t(b) + 8 * s + (s >= 4 ? 64 : 0),
+                                     dV + s * (2048 >> 4), kIdPV, s > 0);
                 // inter-chunk read-out operands: the state after chunk c - 1, Phi'_Q(c)
                 ok = wwait(bar(B_RO_READY), pc);
                 if (!ok) break;
@@ -405,20 +484,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mma_commit_warp(bar(B_FINAL));
             drain_wait(bar(B_FINAL), 0);
         }
-#ifdef LA_TRACE
-    } else if (warp == 3) {
-        // timeline only: completion times of each chunk's MMA groups (observed, not consumed)
-        if (lane == 0 && blockIdx.x == 0) {
-            for (int c = 0; c < n; ++c) {
-                if (c + 1 < n && !mbar_wait(bar(B_T_FULL + ((c + 1) & 1)), (uint32_t)((c + 1) >> 1) & 1u, abort, status)) break;
-                LA_TR(TR_TMA, c, 2);
-                if (!mbar_wait(bar(B_NUM_FULL), (uint32_t)c & 1u, abort, status)) break;
-                LA_TR(TR_TMA, c, 4);
-                if (!mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status)) break;
-                LA_TR(TR_TMA, c, 5);
-            }
+    } else if (warp == 2 || warp == 3) {
+        // ================= P epilogue, keys 64..127 of the rows of lane quarter 2 or 3 =================
+        // (rows 64..127 see up to 128 keys; the P warps 10, 11 take keys 0..63)
+        const int w = warp;
+        const int i = 32 * w + lane;
+        const uint32_t lanebase = (uint32_t)(32 * w) << 16;
+        const int kmin = kPad ? lpad : 0;
+        for (int c = 0; c < n; ++c) {
+            const int b = c & 1;
+            if (!mbar_wait(bar(B_T_FULL + b), (uint32_t)(c >> 1) & 1u, abort, status)) break;
+            __syncwarp();  // tcgen05.ld/st below are warp-collective (.sync.aligned)
+            tc_fence_after();
+            const uint32_t tb = tmem + lanebase + tm_t(b);
+            p_block<kPad, kDecay>(tb, tb + 96, 1, i, w, kmin - c * kC, sb + kSmPow);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PV_READY));
         }
-#endif
     } else if (warp >= 4 && warp < 8) {
         // ================= feature generation (one token per thread) =================
         // and the conversion of state feature groups 3, 4 after each update
@@ -456,6 +539,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if constexpr (kPad) pad = pad || c * kC + t < lpad;
             // the update of chunk c - 1 (S_FULL) released the Phi'_K buffer and V(c - 1)
             if (!mbar_wait(bar(B_S_FULL), pc ^ 1u, abort, status)) break;
+            if (c > 0 && tid == 128) LA_TR(TR_CONV, c - 1, 2);
             if (c > 0 && tid == 128) mbar_arrive(bar(B_V_EMPTY + (c - 1) % kStages));
             if (c > 0) {
                 // state after chunk c - 1, feature groups 3, 4 -> operand of the read-out of c
@@ -488,9 +572,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         if (gen_done && mbar_wait(bar(B_S_FULL), (uint32_t)(n - 1) & 1u, abort, status)) {
             __syncwarp();
             tc_fence_after();
+            if (tid == 128) LA_TR(TR_CONV, n - 1, 4);
             if (wq < 3)
-                store_final_groups(tmem + lanebase + kTmS, 3, 2, 32 * wq + lane, zrow, lane, rows_tab, s0h, s_outh,
-                                   z0h, z_outh, anti_decay);
+                final_groups<true, 3>(tmem + lanebase + kTmS, 32 * wq + lane, zrow, lane, s0h, sb + kSmStage,
+                                      s_outh, z0h, z_outh, anti_decay, std::make_integer_sequence<int, 2>{});
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_STAGED));
+            // every value row is in the image: one bulk copy to s_out
+            if (tid == 128 && s_outh && mbar_wait(bar(B_STAGED), 0u, abort, status)) {
+                bulk_store(s_outh, sb + kSmStage, kStageBytes);
+                bulk_commit();
+                bulk_wait0();
+            }
+            if (tid == 128) LA_TR(TR_CONV, n - 1, 5);
         }
     } else if (warp >= 8 && warp < 12) {
         // ================= P epilogue: P = 1 + T/4 + T^2/32, causal, in place =================
@@ -507,67 +602,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tc_fence_after();
             const uint32_t tb = tmem + lanebase + tm_t(b);
             const int kmin = kPad ? lpad - c * kC : 0;  // keys below kmin are left padding
-            // keys 64 pp .. 64 pp + 63 -> packed columns 32 pp .. 32 pp + 31, written only
-            // after the T columns they overwrite have been read; rows of warp w only see
-            // keys < 32 (w + 1)
-#pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {
-                uint32_t pw[32];
-                if (2 * pp <= w) {
-                    const uint64_t c32 = f2pack(0.03125f, 0.03125f), c4 = f2pack(0.25f, 0.25f),
-                                   c1 = f2pack(1.0f, 1.0f);
-                    const bool diag = 64 * pp + 63 >= 32 * w;  // this block reaches the diagonal
-                    if constexpr (kDecay) {
-                        // in halves of 32 columns: the decay factors (gamma^(i-j), gamma^(i-j-1))
-                        // from the power table need registers too; j > i is masked below
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            uint32_t r[32];
-                            tmem_load32_sync(tb + 64 * pp + 32 * h, r);
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int key = 64 * pp + 32 * h + 2 * j;
-                                const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
-                                const uint64_t f2 = ld_shared_u64(sb + kSmPow + 8u * (uint32_t)max(i - key, 0));
-                                const uint64_t p2 = fmul2(ffma2(t2, ffma2(t2, c32, c4), c1), f2);
-                                float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
-                                if (diag) {
-                                    if (key > i) p0 = 0.f;
-                                    if (key + 1 > i) p1 = 0.f;
-                                }
-                                pw[16 * h + j] = pack_bf16(p0, p1);
-                            }
-                        }
-                    } else {
-                    uint32_t r[64];
-                    tmem_load64_sync(tb + 64 * pp, r);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
-                        uint64_t p2 = ffma2(t2, ffma2(t2, c32, c4), c1);
-                        float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
-                        if (diag) {
-                            const int key = 64 * pp + 2 * j;
-                            if (key > i) p0 = 0.f;
-                            if (key + 1 > i) p1 = 0.f;
-                        }
-                        pw[j] = pack_bf16(p0, p1);
-                    }
-                    }
-                    if (kPad && kmin > 64 * pp) {  // chunk holds left padding: drop padded keys
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int key = 64 * pp + 2 * j;
-                            if (key + 1 < kmin) pw[j] = 0u;
-                            else if (key < kmin) pw[j] &= 0xFFFF0000u;  // low half = the even key
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) pw[j] = 0u;
-                }
-                tmem_store32_sync(tb + 32 * pp, pw);
-            }
+            // keys 0..63 -> packed columns 0..31 of T; keys 64..127 (packed columns
+            // 96..127) of lane quarters 2, 3 are warps 2, 3's share, and rows below
+            // 64 see none of them
+            p_block<kPad, kDecay>(tb, tb, 0, i, w, kmin, sb + kSmPow);
+            if (w < 2) p_block<kPad, kDecay>(tb, tb + 96, 1, i, w, kmin, sb + kSmPow);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PV_READY));
@@ -582,6 +621,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         for (int c = 0; ok && c < n; ++c) {
             if (c + 1 < n && !(ok = do_p(c + 1))) break;
             if (!(ok = mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status))) break;
+            if (tid == 256) LA_TR(TR_CONV, c, 0);
             __syncwarp();
             tc_fence_after();
             const bool last = (c == n - 1);
@@ -592,23 +632,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     __syncwarp();
                     convert_groups<2, 1, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                 } else {
-                    store_final_groups(tmem + lanebase + kTmS, 0, 3, i, zrow, lane, rows_tab, s0h, s_outh, z0h,
-                                       z_outh, anti_decay);
+                    final_groups<true, 0>(tmem + lanebase + kTmS, i, zrow, lane, s0h, sb + kSmStage, s_outh, z0h,
+                                          z_outh, anti_decay, std::make_integer_sequence<int, 3>{});
                 }
                 __syncwarp();
             }
-            if (!last) {
+            if (last) {
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_STAGED));
+            } else {
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_RO_READY));
             }
+            if (tid == 256) LA_TR(TR_CONV, c, 1);
         }
     } else if (warp >= 12) {
         // ========== output epilogue y = num / den ==========
         const int w = warp - 12;
-        const int i = 32 * w + lane;          // query row (num lane) / value row d of S'^T
-        const bool zrow = (w == 2);           // warp 14: lane 64 holds z'
+        const int i = 32 * w + lane;          // query row (num lane)
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
         // PV_READY(c) from the y warps: num drained after chunk c - 1, and (one
         // lane) the loads P V(c) and Q K^T(c + 1) read, observed in order
@@ -661,7 +705,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             if (tid == 384) LA_TR(TR_EPI, c, 3);
         }
+        if (tid == 384) LA_TR(TR_CONV, n - 1, 6);
         if (lane == 0) bulk_wait0();  // y stores complete before the CTA exits
+        if (tid == 384) LA_TR(TR_CONV, n - 1, 7);
     }
 
     tc_fence_before();

@@ -31,8 +31,7 @@ constexpr uint32_t kSmPhiK = 0;        // MN-major B: 3 x 16K SW128
 constexpr uint32_t kSmV = 49152;       // 2 x [128][64] bf16 SW128
 constexpr uint32_t kSmOnes = 81920;    // [128][64] bf16 ones (rows 64..127 of [V | 1]^T)
 constexpr uint32_t kSmK = 98304;       // 2 x [128][16] bf16 SW32
-constexpr uint32_t kSmRows = 106496;   // [160] x int4 feature -> ABI row table
-constexpr uint32_t kSmBar = kSmRows + 160 * 16;
+constexpr uint32_t kSmBar = 106496;
 constexpr uint32_t kSmTotal = kSmBar + 256;
 constexpr uint32_t kSmAlloc = kSmTotal + 1024;
 
@@ -54,7 +53,6 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
     const uint32_t sb = smem_u32(smem);
     auto bar = [&](int i) { return sb + kSmBar + 8u * (uint32_t)i; };
     volatile int *abort = reinterpret_cast<volatile int *>(smem + kSmAbort);
-    const int4 *rows_tab = reinterpret_cast<const int4 *>(smem + kSmRows);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t bh = blockIdx.x;
@@ -82,10 +80,6 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
     }
     for (int i = tid; i < 16384 / 16; i += kThreads)
         st_shared_v4(sb + kSmOnes + 16 * i, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
-    if (tid < kNFeat) {
-        const Rows r = abi_rows(tid);
-        reinterpret_cast<int4 *>(smem + kSmRows)[tid] = make_int4(r.r1, r.r2, r.kind, 0);
-    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -160,8 +154,9 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
             tc_fence_after();
             if (ok && n > 0) {
                 const int64_t slot = bh * nseg + seg;
-                store_final_groups(tmem + ((uint32_t)(32 * w) << 16), 0, kNFeat / 32, 32 * w + lane, zrow, lane,
-                                   rows_tab, nullptr, part_s + slot * kD * kDV, nullptr, part_z + slot * kD, 1.f);
+                final_groups<false, 0>(tmem + ((uint32_t)(32 * w) << 16), 32 * w + lane, zrow, lane, nullptr, 0u,
+                                       part_s + slot * kD * kDV, nullptr, part_z + slot * kD, 1.f,
+                                       std::make_integer_sequence<int, kNFeat / 32>{});
             }
         }
     }

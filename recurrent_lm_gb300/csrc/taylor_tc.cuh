@@ -152,7 +152,7 @@ __device__ __forceinline__ void load_row16_raw(uint32_t tile, int t, uint4 &lo, 
 // ABI row(s) of compact feature f: r1, r2 (r2 < 0 if none); kind 0 = square,
 // 1 = off-diagonal pair, 2 = constant / linear, 3 = padding.
 struct Rows { int r1, r2, kind; };
-__device__ __forceinline__ Rows abi_rows(int f) {
+__host__ __device__ constexpr Rows abi_rows(int f) {
     const int r = f >> 1, e = f & 1;
     const PairSpec p = pair_spec(r);
     if (p.kind <= 2) {
@@ -165,38 +165,89 @@ __device__ __forceinline__ Rows abi_rows(int f) {
     if (p.kind == 4 && e == 0) return {0, -1, 2};
     return {-1, -1, 3};
 }
+static_assert(abi_rows(0).r1 == 17 && abi_rows(152).r1 == 0 && abi_rows(153).kind == 3, "feature order");
 
-// Compact entries of the initial state for the 32 features of one row group
-// (rows table entries e[0..31]): squares carry 1/sqrt2, pairs the symmetric
-// sum over (a,b) and (b,a) times 1/sqrt2.  The loads are unconditional
-// (padding reads row 0, unpaired features read their row twice) and all issued
-// before any is used, so each half's 32 reads are in flight together instead of
-// paying one DRAM latency each.
-__device__ __forceinline__ void compact_initial_group(const float *col, int stride, const int4 *e,
-                                                      uint32_t (&r)[32]) {
+// The conversions between the 273-row ABI state and the compact rows are
+// written per feature with the feature index F as a template argument, so the
+// kind and the ABI rows of every feature are compile-time constants (no row
+// table, no branches, no dummy loads).
+
+// Reads of the ABI column `col` (rows `stride` elements apart) that compact
+// feature F needs: its row, and for an off-diagonal pair the mirrored row.
+template <int F>
+__device__ __forceinline__ void abi_reads(const float *col, int64_t stride, float &a, float &b) {
+    constexpr Rows e = abi_rows(F);
+    a = b = 0.f;
+    if constexpr (e.kind != 3) a = __ldcg(col + e.r1 * stride);
+    if constexpr (e.kind == 1) b = __ldcg(col + e.r2 * stride);
+}
+
+// Compact entry of feature F: squares carry 1/sqrt2, pairs the symmetric sum
+// over (a,b) and (b,a) times 1/sqrt2.
+template <int F>
+__device__ __forceinline__ uint32_t compact_entry(float a, float b) {
+    constexpr Rows e = abi_rows(F);
+    if constexpr (e.kind == 3) return 0u;
+    else if constexpr (e.kind == 2) return __float_as_uint(a);
+    else if constexpr (e.kind == 0) return __float_as_uint(a * kRSqrt2);
+    else return __float_as_uint((a + b) * kRSqrt2);
+}
+
+// Compact entries of the initial state for the 32 features of group G from
+// the ABI column `col` (NULL: zero state).  Every read is issued before any is
+// used, so they are in flight together.
+template <int G, int... J>
+__device__ __forceinline__ void compact_initial_group(const float *col, int64_t stride, uint32_t (&r)[32],
+                                                      std::integer_sequence<int, J...>) {
     if (!col) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = 0u;
+        ((r[J] = 0u), ...);
         return;
     }
-#pragma unroll
-    for (int h = 0; h < 32; h += 16) {  // two halves of 16 features: fewer live registers
-        float a[16], b[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int4 t = e[h + j];
-            const int r1 = t.z == 3 ? 0 : t.x;
-            const int r2 = t.z == 1 ? t.y : r1;
-            a[j] = __ldg(col + (int64_t)r1 * stride);
-            b[j] = __ldg(col + (int64_t)r2 * stride);
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int k = e[h + j].z;
-            const float x = k == 3 ? 0.f : k == 2 ? a[j] : k == 0 ? a[j] * kRSqrt2 : (a[j] + b[j]) * kRSqrt2;
-            r[h + j] = __float_as_uint(x);
-        }
+    float a[32], b[32];
+    (abi_reads<32 * G + J>(col, stride, a[J], b[J]), ...);
+    ((r[J] = compact_entry<32 * G + J>(a[J], b[J])), ...);
+}
+
+// ABI value(s) of compact feature F with entry x: the rows' values, the
+// antisymmetric part anti (of a pair) added to (a,b) and subtracted from (b,a).
+// kStage: written into a shared-memory image at stage_d + 4 * 64 * row (value
+// column d: rows 256 bytes apart), else to out[row * stride] in global memory.
+template <bool kStage, int F>
+__device__ __forceinline__ void abi_write(float x, float anti, uint32_t stage_d, float *out, int64_t stride) {
+    constexpr Rows e = abi_rows(F);
+    if constexpr (e.kind == 3) return;
+    float v1, v2 = 0.f;
+    if constexpr (e.kind == 2) v1 = x;
+    else if constexpr (e.kind == 0) v1 = x * kSqrt2;
+    else {
+        v1 = x * kRSqrt2 + anti;
+        v2 = x * kRSqrt2 - anti;
     }
+    if constexpr (kStage) {
+        st_shared_f32(stage_d + 256u * (uint32_t)e.r1, v1);
+        if constexpr (e.kind == 1) st_shared_f32(stage_d + 256u * (uint32_t)e.r2, v2);
+    } else {
+        out[e.r1 * stride] = v1;
+        if constexpr (e.kind == 1) out[e.r2 * stride] = v2;
+    }
+}
+
+// One group G of the final ABI state from its compact entries r: the
+// antisymmetric part of the initial state's column col0 (NULL: none), scaled
+// by anti_scale, is read for the pairs (all reads issued together) and added.
+template <bool kStage, int G, int... J>
+__device__ __forceinline__ void final_group(const uint32_t (&r)[32], const float *col0, int64_t stride,
+                                            float anti_scale, uint32_t stage_d, float *out,
+                                            std::integer_sequence<int, J...>) {
+    float a[32], b[32];
+    if (col0) {
+        (abi_reads<32 * G + J>(col0, stride, a[J], b[J]), ...);
+    } else {
+        ((a[J] = 0.f), ...);
+        ((b[J] = 0.f), ...);
+    }
+    const float h = 0.5f * anti_scale;
+    (abi_write<kStage, 32 * G + J>(__uint_as_float(r[J]), h * (a[J] - b[J]), stage_d, out, stride), ...);
 }
 
 // Drain wait used when unwinding: bounded, ignores the abort flag.
@@ -206,57 +257,34 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
         if (clock64() - t0 > kWaitCycles) return;
 }
 
-// Final ABI state from TMEM rows, for one warp's lanes and feature groups
-// [g0, g0 + ng): value rows d < 64 (column d of each ABI row), and the z' row
-// (lane 64, by lane 0 of the warp that owns lanes 64..95).  Each group's reads
-// of the initial state are issued together before its stores.  Runs once per
-// CTA, so it is kept out of line.
-static __device__ __noinline__ void store_final_groups(uint32_t taddr, int g0, int ng, int d, bool zrow, int lane,
-                                                       const int4 *rows_tab, const float *s0h, float *s_outh,
-                                                       const float *z0h, float *z_outh, float anti_scale) {
-    const float *col0 = zrow ? z0h : (s0h ? s0h + d : nullptr);
-    float *out = zrow ? z_outh : (s_outh ? s_outh + d : nullptr);
-    const int64_t stride = zrow ? 1 : kDV;
-    for (int g = g0; g < g0 + ng; ++g) {
-        uint32_t r[32];
-        tmem_load32_sync(taddr + 32 * g, r);
-        if (out && (!zrow || lane == 0)) {
-            // antisymmetric part of the initial state for the pairs: unconditional
-            // loads (other features read row 0 and discard it) so all are in flight at once
-            float anti[32];
-            if (col0) {
-                float a[32], b[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int4 e = rows_tab[32 * g + j];
-                    const int r1 = e.z == 1 ? e.x : 0, r2 = e.z == 1 ? e.y : 0;
-                    a[j] = __ldg(col0 + r1 * stride);
-                    b[j] = __ldg(col0 + r2 * stride);
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    anti[j] = rows_tab[32 * g + j].z == 1 ? (0.5f * anti_scale) * (a[j] - b[j]) : 0.f;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) anti[j] = 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int4 e = rows_tab[32 * g + j];
-                const float x = __uint_as_float(r[j]);
-                if (e.z == 2) {
-                    out[e.x * stride] = x;
-                } else if (e.z == 0) {
-                    out[e.x * stride] = x * kSqrt2;
-                } else if (e.z == 1) {
-                    const float sym = x * kRSqrt2;
-                    out[e.x * stride] = sym + anti[j];
-                    out[e.y * stride] = sym - anti[j];
-                }
-            }
-        }
-        __syncwarp();
+// Final ABI state of feature group G from TMEM rows, for one warp's lanes:
+// value rows (column d of each ABI row) and the z' row (lane 64, by lane 0 of
+// the warp that owns lanes 64..95).  The value rows go to the shared-memory
+// image at `stage` (kStage, a [273][64] fp32 array) or to s_outh; z' goes to
+// z_outh.  A NULL destination is skipped.
+template <bool kStage, int G>
+__device__ __forceinline__ void final_group_rows(uint32_t taddr, int d, bool zrow, int lane, const float *s0h,
+                                                 uint32_t stage, float *s_outh, const float *z0h, float *z_outh,
+                                                 float anti_scale) {
+    const auto js = std::make_integer_sequence<int, 32>{};
+    uint32_t r[32];
+    tmem_load32_sync(taddr + 32 * G, r);
+    if (zrow) {
+        if (lane == 0 && z_outh) final_group<false, G>(r, z0h, 1, anti_scale, 0u, z_outh, js);
+    } else if (kStage || s_outh) {
+        final_group<kStage, G>(r, s0h ? s0h + d : nullptr, kDV, anti_scale, stage + 4u * (uint32_t)d,
+                               s_outh ? s_outh + d : nullptr, js);
     }
+    __syncwarp();
+}
+
+// Feature groups G0 + I... of the final ABI state (see final_group_rows).  Runs
+// once per CTA, so it is kept out of line.
+template <bool kStage, int G0, int... I>
+static __device__ __noinline__ void final_groups(uint32_t taddr, int d, bool zrow, int lane, const float *s0h,
+                                                 uint32_t stage, float *s_outh, const float *z0h, float *z_outh,
+                                                 float anti_scale, std::integer_sequence<int, I...>) {
+    (final_group_rows<kStage, G0 + I>(taddr, d, zrow, lane, s0h, stage, s_outh, z0h, z_outh, anti_scale), ...);
 }
 
 }  // namespace taylor
