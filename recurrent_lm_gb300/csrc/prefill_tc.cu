@@ -28,10 +28,14 @@
 //    influence any output and is passed through unchanged).
 //  * These MMAs have small N and are bound by shared-memory operand
 //    bandwidth, so the layout minimises operand bytes per chunk.
-//  * Roles: warp 0 TMA producer (q, k, v chunks, zero-filled past N), warp 1
-//    MMA issuer, warpgroup 1 feature generation (one token per thread),
-//    warpgroup 2 P epilogue, warpgroup 3 output epilogue y = num / den and
-//    the state conversion (TMEM fp32 -> bf16 operand, final state store).
+//  * Roles: warp 0 TMA producer (q, k, v chunks, zero-filled past N; warp 3
+//    issues the first chunks' loads during set-up), warp 1 MMA issuer,
+//    warps 2, 3 the P epilogue of keys 64..127 for rows 64..127, warpgroup 1
+//    feature generation (one token per thread) and the state conversion
+//    (TMEM fp32 -> bf16 operand) of feature groups 3, 4, warpgroup 2 the P
+//    epilogue of keys 0..63 and the conversion of groups 0..2, warpgroup 3
+//    the output epilogue y = num / den (TMA stores).  The final state is
+//    assembled in shared memory and written with one bulk copy.
 //  * Every wait is bounded: after ~1 s the kernel records a timeout in the
 //    device status word and every role unwinds.
 #include <type_traits>
@@ -314,7 +318,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 
     // decay: the head's gamma (clamped to [0, 1]; out of range is reported) and
     // its powers (gamma^d, gamma^(d-1)) for d = 0..128
-    auto pow_gamma = [&](int d) { return kDecay ? reinterpret_cast<const float2 *>(smem + kSmPow)[d].x : 1.f; };
+    auto pow_gamma = [&](int d) {
+        return kDecay ? __uint_as_float((uint32_t)ld_shared_u64(sb + kSmPow + 8u * (uint32_t)d)) : 1.f;
+    };
     if constexpr (kDecay) {
         float g = gamma[bh % H];
         if (!(g >= 0.f && g <= 1.f)) {
@@ -330,6 +336,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     auto chunk_len = [&](int c) { return min(kC, N - c * kC); };
     // the antisymmetric part of s0 bypasses the compact state: it decays by gamma^N
     const float anti_decay = kDecay ? powf(pow_gamma(1), (float)N) : 1.f;
+
+    // the first kStages chunks' loads (their stages start empty) go out now, so
+    // that they land while the initial state is read; warp 3 has no state rows
+    // (not in the decayed variant, whose registers are already tight)
+    const int n_early = kDecay ? 0 : (n < kStages ? n : kStages);
+    if (!kDecay && warp == 3 && lane == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        for (int c = 0; c < n_early; ++c) {
+            mbar_expect_tx(bar(B_QK_FULL + c), 2 * kC * 16 * 2);
+            tma_load_3d(sb + kSmQ + c * 4096, &tq, bar(B_QK_FULL + c), 0, c * kC, (int)bh);
+            tma_load_3d(sb + kSmK + c * 4096, &tk, bar(B_QK_FULL + c), 0, c * kC, (int)bh);
+            mbar_expect_tx(bar(B_V_FULL + c), kC * 64 * 2);
+            tma_load_3d(sb + kSmV + c * 16384, &tv, bar(B_V_FULL + c), 0, c * kC, (int)bh);
+        }
+    }
 
     // initial state, before any role starts: S'^T rows (values d = 0..63, TMEM lane
     // quarters 0, 1) and z' (lane 64, quarter 2) in TMEM, and their bf16 operand
@@ -373,11 +396,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (warp == 0) {
         // ================= TMA producer =================
         if (lane == 0) {
-            prefetch_tmap(&tq);
-            prefetch_tmap(&tk);
-            prefetch_tmap(&tv);
-            int issued_qk = 0, issued_v = 0;
-            for (int c = 0; c < n; ++c) {
+            if (kDecay) {
+                prefetch_tmap(&tq);
+                prefetch_tmap(&tk);
+                prefetch_tmap(&tv);
+            }
+            int issued_qk = n_early, issued_v = n_early;
+            for (int c = n_early; c < n; ++c) {
                 const int st = c % kStages;
                 const uint32_t ph = ((uint32_t)(c / kStages) & 1u) ^ 1u;
                 if (!mbar_wait(bar(B_QK_EMPTY + st), ph, abort, status)) break;
@@ -391,6 +416,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 mbar_expect_tx(bar(B_V_FULL + st), kC * 64 * 2);
                 tma_load_3d(sb + kSmV + st * 16384, &tv, bar(B_V_FULL + st), 0, c * kC, (int)bh);
                 issued_v = c + 1;
+                if (c == n - 1 && s0h) {
+                    // the final state store reads s0 again (its antisymmetric part)
+                    prefetch_l2_bulk(s0h, (uint32_t)kD * kDV * 4);
+                    for (int o = 0; o < kD; o += 32) prefetch_l2(z0h + o);
+                }
             }
             if (*abort) {
                 // every issued load must land before the CTA may exit; the last
@@ -677,7 +707,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tmem_load64_1_sync(tmem + lanebase + kTmNum, 64, r, dr);
                 tc_fence_before();
                 __syncwarp();
-                ok = pv_ready(c + 1);  // num of chunk c drained
+                ok = __all_sync(0xffffffffu, pv_ready(c + 1));  // num of chunk c drained (warp-uniform result)
                 // y rows of this warp -> its 4 KB staging tile -> one bulk tensor store
                 // (rows past N are clipped by the store)
                 float inv = 1.0f / (__uint_as_float(dr) + eps);
