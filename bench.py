@@ -18,9 +18,10 @@ times the other two calls of the path, reported under ``legs``:
     one CUDA graph, state from a 2048-token prefill (tokens/s and HBM GB/s).
 Inputs are seeded synthetic tensors already resident in HBM and larger than
 L2 (2.1 GB of q/k/v per prefill step; the 145 MB decode state is read and
-written every step).  ``e2e`` times the same prefill through the C-ABI with
-pinned host buffers, host->device copies of q, k, v, s0, z0 and
-device->host copies of y, s, z inside the timed region.
+written every step).  ``e2e`` times the same prefill through the C-ABI's
+host-memory call (la_prefill_host) with pinned host buffers: host->device
+copies of q, k, v, s0, z0 and device->host copies of y, s, z inside the timed
+region, overlapped with the kernels over slices of (b, h) rows.
 
 Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no
 collective on the data path); the timed region is bracketed by barriers and
@@ -269,24 +270,19 @@ def leg_prefill(la, args, dist, dev, clocks):
 
 
 def e2e_prefill(la, args, dist, q, k, v, s0, z0):
-    """Same prefill through the C-ABI from pinned host buffers: H2D of the
-    inputs and D2H of y, s, z inside the timed region."""
+    """Same prefill through the C-ABI's host-memory call (la_prefill_host) from
+    pinned host buffers: the H2D copies of the inputs and the D2H copies of y,
+    s, z are inside the timed region, pipelined with the kernels over slices
+    of (b, h) rows."""
     hq, hk, hv, hs0, hz0 = (t.cpu().pin_memory() for t in (q, k, v, s0, z0))
-    dq, dk, dv_, ds0, dz0 = (torch.empty_like(t) for t in (q, k, v, s0, z0))
     B, H, N = q.shape[:3]
-    y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=q.device)
-    s = torch.empty_like(s0)
-    z = torch.empty_like(z0)
-    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    hs = torch.empty(s.shape, dtype=s.dtype).pin_memory()
-    hz = torch.empty(z.shape, dtype=z.dtype).pin_memory()
+    hy = torch.empty((B, H, N, 64), dtype=torch.bfloat16).pin_memory()
+    hs = torch.empty(s0.shape, dtype=s0.dtype).pin_memory()
+    hz = torch.empty(z0.shape, dtype=z0.dtype).pin_memory()
+    ws = torch.empty(la.prefill_host_workspace_size(B, H, N), dtype=torch.uint8, device=q.device)
 
     def step():
-        for d, h in ((dq, hq), (dk, hk), (dv_, hv), (ds0, hs0), (dz0, hz0)):
-            d.copy_(h, non_blocking=True)
-        la.prefill(dq, dk, dv_, ds0, dz0, y=y, s_out=s, z_out=z)
-        for h, d in ((hy, y), (hs, s), (hz, z)):
-            h.copy_(d, non_blocking=True)
+        la.prefill_host(hq, hk, hv, hs0, hz0, y=hy, s_out=hs, z_out=hz, workspace=ws)
 
     steps = max(1, min(args.steps, 5))
     ms = time_loop(step, steps, max(1, min(args.warmup, 2)), dist)

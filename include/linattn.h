@@ -17,7 +17,8 @@
  * f = 17 + 16 a + b quadratic (a, b in 0..15).
  *
  * Common conventions for every entry point:
- *  - Every data pointer is a DEVICE pointer to a dense row-major array;
+ *  - Every data pointer is a DEVICE pointer to a dense row-major array
+ *    (la_prefill_host: activations and states in host memory, see there);
  *    the caller owns and allocates every buffer.  The library allocates no
  *    memory and keeps no state between calls (apart from the device status
  *    word read by la_check_device_status).
@@ -102,6 +103,39 @@ LA_API la_status la_prefill(const void *q, const void *k, const void *v,
                      void *y, float *s_out, float *z_out,
                      int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
                      la_dtype dtype, float eps, la_stream_t stream);
+
+/*
+ * la_prefill_host -- la_prefill for activations and states that live in host
+ * memory: the same computation, with the host <-> device copies inside the
+ * call and overlapped with the kernels.
+ *
+ * q, k, v, s0, z0, y, s_out, z_out have la_prefill's shapes, dtypes and
+ * NULL rules, but may be any memory the CUDA runtime can address (copies use
+ * cudaMemcpyDefault).  For the copies to overlap they must be page-locked
+ * (cudaHostAlloc / cudaHostRegister); pageable memory gives correct results
+ * without the overlap.  No alignment is required of them.
+ *
+ * workspace: DEVICE buffer of at least la_prefill_host_workspace_size(B, H,
+ * N, d_feat, dtype) bytes, 256-byte aligned, owned by the caller; it holds the
+ * device copies of the slices in flight.  The (b, h) rows are processed in up
+ * to 8 slices, up to 3 at a time, each on a stream created for the call (with
+ * events ordering it after the work already on `stream` and `stream` after
+ * it); streams and events are released when their work completes.
+ *
+ * The call returns once the work is enqueued: the host outputs are valid
+ * after `stream` has reached this point (cudaStreamSynchronize).  The inputs
+ * must stay unchanged, and the outputs untouched, until then.
+ * d_feat 8/16/24/32 and both dtypes as la_prefill; no padding or decay.
+ * Errors as la_prefill; a workspace that is too small is LA_ERR_INVALID_ARG.
+ */
+LA_API size_t la_prefill_host_workspace_size(int64_t B, int64_t H, int64_t N, int d_feat,
+                                             la_dtype dtype);
+LA_API la_status la_prefill_host(const void *q, const void *k, const void *v,
+                          const float *s0, const float *z0,
+                          void *y, float *s_out, float *z_out,
+                          void *workspace, size_t workspace_bytes,
+                          int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                          la_dtype dtype, float eps, la_stream_t stream);
 
 /*
  * la_prefix_workspace_size -- bytes of device scratch la_prefix_prefill

@@ -50,6 +50,9 @@ SIGNATURES = {
     "la_decode_step_decay": (_I, [_VP, _VP, _VP, _FP, _FP, _FP, _FP, _FP, _VP, _I64, _I64, _I, _I,
                                   _I, _F, _VP]),
     "la_prefix_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "la_prefill_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _I]),
+    "la_prefill_host": (_I, [_VP, _VP, _VP, _FP, _FP, _VP, _FP, _FP, _VP, _SZ, _I64, _I64, _I64,
+                             _I, _I, _I, _F, _VP]),
     "la_prefix_prefill": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _FP, _FP, _VP,
                                _SZ, _I64, _I64, _I64, _I, _I, _I, _F, _VP]),
     "la_prefix_prefill_padded": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _VP, _FP, _FP,
@@ -174,6 +177,67 @@ def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
         _raise(lib.la_prefill_padded(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(left_pad),
                                      _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, dk, D_V, _dt(q),
                                      float(eps), _stream(stream)))
+    return y, s_out, z_out
+
+
+def _need_host(t: torch.Tensor, name: str, shape, dtype):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a CPU tensor (prefill_host reads and writes host memory)")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def prefill_host_workspace_size(B: int, H: int, N: int, dk: int = D_FEAT,
+                                dtype: torch.dtype = torch.bfloat16) -> int:
+    dt = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
+    return int(load_library().la_prefill_host_workspace_size(B, H, N, dk, dt))
+
+
+def prefill_host(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None, z_out=None,
+                 want_state: bool = True, workspace=None, stream=None, device=None):
+    """Causal prefill from and to host memory (la_prefill_host): q, k, v and
+    s0, z0 are CPU tensors (pinned, for the copies to overlap the kernels);
+    outputs are CPU tensors, pinned when allocated here.  ``workspace`` is a
+    CUDA uint8 tensor of at least prefill_host_workspace_size(...) bytes on
+    ``device`` (the current CUDA device if None; allocated here if not given).
+    The call is asynchronous: the host outputs are valid once ``stream`` (the
+    current stream if None) has completed the call's work."""
+    lib = load_library()
+    B, H, N, dk = q.shape
+    D = feature_dim(dk)
+    dt = q.dtype
+    _need_host(q, "q", (B, H, N, dk), dt)
+    _need_host(k, "k", (B, H, N, dk), dt)
+    _need_host(v, "v", (B, H, N, D_V), dt)
+    if s0 is not None or z0 is not None:
+        _need_host(s0, "s0", (B, H, D, D_V), torch.float32)
+        _need_host(z0, "z0", (B, H, D), torch.float32)
+    if y is None:
+        y = torch.empty((B, H, N, D_V), dtype=dt).pin_memory()
+    _need_host(y, "y", (B, H, N, D_V), dt)
+    if want_state:
+        if s_out is None:
+            s_out = torch.empty((B, H, D, D_V), dtype=torch.float32).pin_memory()
+        if z_out is None:
+            z_out = torch.empty((B, H, D), dtype=torch.float32).pin_memory()
+    if s_out is not None:
+        _need_host(s_out, "s_out", (B, H, D, D_V), torch.float32)
+    if z_out is not None:
+        _need_host(z_out, "z_out", (B, H, D), torch.float32)
+    if workspace is None:
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        need = prefill_host_workspace_size(B, H, N, dk, dt)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", (workspace.numel(),), torch.uint8)
+    _raise(lib.la_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
+                               _ptr(z_out), _ptr(workspace), workspace.numel(), B, H, N, dk, D_V,
+                               _dt(q), float(eps), _stream(stream)))
     return y, s_out, z_out
 
 

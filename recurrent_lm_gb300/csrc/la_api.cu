@@ -353,6 +353,139 @@ la_status la_prefill_decay(const void *q, const void *k, const void *v, const fl
                         stream, gamma);
 }
 
+}  // extern "C"
+
+namespace {
+
+// la_prefill_host: the (b, h) rows are processed in up to kHostSlices slices;
+// kHostBuffers slices are in flight at once, each on its own stream with its
+// own device buffers (copy in, compute, copy out), so the two copy directions
+// and the kernels overlap.
+constexpr int64_t kHostSlices = 8;
+constexpr int64_t kHostBuffers = 3;
+
+struct HostSliceLayout {
+    size_t q, k, v, y, s0, z0, s, z, total;
+};
+
+HostSliceLayout host_slice_layout(int64_t R, int64_t N, int dk, size_t es) {
+    const int64_t D = la::feat_dim(dk);
+    HostSliceLayout L{};
+    size_t off = 0;
+    L.q = off; off = align256(off + es * R * N * dk);
+    L.k = off; off = align256(off + es * R * N * dk);
+    L.v = off; off = align256(off + es * R * N * kDV);
+    L.y = off; off = align256(off + es * R * N * kDV);
+    L.s0 = off; off = align256(off + sizeof(float) * R * D * kDV);
+    L.z0 = off; off = align256(off + sizeof(float) * R * D);
+    L.s = off; off = align256(off + sizeof(float) * R * D * kDV);
+    L.z = off; off = align256(off + sizeof(float) * R * D);
+    L.total = off;
+    return L;
+}
+
+int64_t host_slice_rows(int64_t BH) { return (BH + kHostSlices - 1) / kHostSlices; }
+
+size_t host_workspace_bytes(int64_t BH, int64_t N, int dk, size_t es) {
+    const int64_t R = host_slice_rows(BH);
+    const int64_t nslice = (BH + R - 1) / R;
+    const int64_t nb = nslice < kHostBuffers ? nslice : kHostBuffers;
+    return (size_t)nb * host_slice_layout(R, N, dk, es).total;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t la_prefill_host_workspace_size(int64_t B, int64_t H, int64_t N, int d_feat, la_dtype dtype) {
+    if (check_common(B, H, N, d_feat, kDV, dtype) != LA_OK) return 0;
+    return host_workspace_bytes(B * H, N, d_feat, esize(dtype));
+}
+
+la_status la_prefill_host(const void *q, const void *k, const void *v, const float *s0,
+                          const float *z0, void *y, float *s_out, float *z_out, void *workspace,
+                          size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int d_feat,
+                          int d_v, la_dtype dtype, float eps, la_stream_t stream) {
+    la_status st = check_common(B, H, N, d_feat, d_v, dtype);
+    if (st != LA_OK) return st;
+    if ((s0 == nullptr) != (z0 == nullptr)) return LA_ERR_INVALID_ARG;
+    if (N > 0 && (!q || !k || !v || !y)) return LA_ERR_INVALID_ARG;
+    const int64_t BH = B * H;
+    const size_t es = esize(dtype);
+    const int64_t D = la::feat_dim(d_feat);
+    if (!workspace || workspace_bytes < host_workspace_bytes(BH, N, d_feat, es)) return LA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LA_ERR_MISALIGNED;
+    const Range in[] = {{q, es * BH * N * d_feat}, {k, es * BH * N * d_feat}, {v, es * BH * N * kDV},
+                        {s0, sizeof(float) * BH * D * kDV}, {z0, sizeof(float) * BH * D}};
+    const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * D * kDV},
+                         {z_out, sizeof(float) * BH * D}};
+    if (any_overlap(in, 5, out, 3)) return LA_ERR_INVALID_ARG;
+    int dev;
+    unsigned *status;
+    if ((st = device_setup(&dev, &status)) != LA_OK) return st;
+
+    const int64_t R = host_slice_rows(BH);
+    const int64_t nslice = (BH + R - 1) / R;
+    const int nb = (int)(nslice < kHostBuffers ? nslice : kHostBuffers);
+    const HostSliceLayout L = host_slice_layout(R, N, d_feat, es);
+    cudaStream_t caller = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t ss[kHostBuffers] = {};
+    cudaEvent_t fork = nullptr, join[kHostBuffers] = {};
+    bool ok = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int j = 0; ok && j < nb; ++j)
+        ok = cudaStreamCreateWithFlags(&ss[j], cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&join[j], cudaEventDisableTiming) == cudaSuccess;
+    // the internal streams start after the caller's earlier work
+    ok = ok && cudaEventRecord(fork, caller) == cudaSuccess;
+    for (int j = 0; ok && j < nb; ++j) ok = cudaStreamWaitEvent(ss[j], fork, 0) == cudaSuccess;
+    la_status result = ok ? LA_OK : LA_ERR_CUDA;
+    auto copy = [&](void *dst, const void *src, size_t bytes, cudaStream_t cs) {
+        if (result == LA_OK && bytes > 0 && cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, cs) != cudaSuccess)
+            result = LA_ERR_CUDA;
+    };
+    for (int64_t i = 0; ok && result == LA_OK && i < nslice; ++i) {
+        const int j = (int)(i % nb);
+        cudaStream_t cs = ss[j];
+        char *base = static_cast<char *>(workspace) + (size_t)j * L.total;
+        const int64_t r0 = i * R, nr = (BH - r0) < R ? (BH - r0) : R;
+        const size_t qk = es * N * d_feat, vy = es * N * kDV, sr = sizeof(float) * D * kDV,
+                     zr = sizeof(float) * D;
+        copy(base + L.q, static_cast<const char *>(q) + r0 * qk, nr * qk, cs);
+        copy(base + L.k, static_cast<const char *>(k) + r0 * qk, nr * qk, cs);
+        copy(base + L.v, static_cast<const char *>(v) + r0 * vy, nr * vy, cs);
+        if (s0) {
+            copy(base + L.s0, reinterpret_cast<const char *>(s0) + r0 * sr, nr * sr, cs);
+            copy(base + L.z0, reinterpret_cast<const char *>(z0) + r0 * zr, nr * zr, cs);
+        }
+        if (result != LA_OK) break;
+        // the slice's rows as nr independent sequences of one batch row each
+        result = prefill_impl(base + L.q, base + L.k, base + L.v,
+                              s0 ? reinterpret_cast<float *>(base + L.s0) : nullptr,
+                              s0 ? reinterpret_cast<float *>(base + L.z0) : nullptr, nullptr, base + L.y,
+                              s_out ? reinterpret_cast<float *>(base + L.s) : nullptr,
+                              z_out ? reinterpret_cast<float *>(base + L.z) : nullptr, nr, 1, N, d_feat,
+                              d_v, dtype, eps, reinterpret_cast<la_stream_t>(cs));
+        copy(static_cast<char *>(y) + r0 * vy, base + L.y, nr * vy, cs);
+        if (s_out) copy(reinterpret_cast<char *>(s_out) + r0 * sr, base + L.s, nr * sr, cs);
+        if (z_out) copy(reinterpret_cast<char *>(z_out) + r0 * zr, base + L.z, nr * zr, cs);
+    }
+    // the caller's stream continues after every slice (also after a failure,
+    // so that no enqueued copy outlives the call's ordering)
+    for (int j = 0; j < nb; ++j) {
+        if (ss[j] && join[j] && cudaEventRecord(join[j], ss[j]) == cudaSuccess)
+            cudaStreamWaitEvent(caller, join[j], 0);
+        else if (ss[j])
+            cudaStreamSynchronize(ss[j]);
+    }
+    // released once their work completes
+    for (int j = 0; j < nb; ++j) {
+        if (join[j]) cudaEventDestroy(join[j]);
+        if (ss[j]) cudaStreamDestroy(ss[j]);
+    }
+    if (fork) cudaEventDestroy(fork);
+    return result;
+}
+
 la_status la_check_device_status(la_stream_t stream) {
     int dev;
     unsigned *status;

@@ -193,3 +193,36 @@ def test_padding_decay_and_prefix_need_d16(lib):
                                  1, 1, 8, 32, 64, 1, 0.0, None) == binding.LA_ERR_UNSUPPORTED
     assert lib.la_decode_step_decay(q, k, v, fake(9), s0, z0, so, zo, y, 1, 1, 8, 64, 1, 0.0,
                                     None) == binding.LA_ERR_UNSUPPORTED
+
+
+def test_host_prefill_workspace_size(lib):
+    need = lib.la_prefill_host_workspace_size(2, 3, 300, 16, 1)
+    assert need > 0 and need % 256 == 0
+    # three slices of one row in flight: q, k, v, y and both states per slice
+    per_row = 2 * 300 * (16 + 16 + 64 + 64) + 4 * (273 * 64 + 273) * 2
+    assert 3 * per_row <= need <= 3 * per_row + 3 * 8 * 256
+    assert lib.la_prefill_host_workspace_size(0, 3, 300, 16, 1) == 0
+    assert lib.la_prefill_host_workspace_size(2, 3, 300, 12, 1) == 0
+    assert lib.la_prefill_host_workspace_size(2, 3, 300, 16, 1) < lib.la_prefill_host_workspace_size(2, 3, 300, 16, 0)
+
+
+def call_host(lib, p, ws, ws_bytes, B=2, H=3, N=300, dk=16, dtype=1):
+    return lib.la_prefill_host(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], ws, ws_bytes, B, H, N,
+                               dk, 64, dtype, 0.0, None)
+
+
+def test_host_prefill_rejects_bad_args(lib):
+    need = lib.la_prefill_host_workspace_size(2, 3, 300, 16, 1)
+    p = [fake(i) for i in range(8)]
+    ws = fake(9)
+    assert call_host(lib, p, ws, need - 1) == binding.LA_ERR_INVALID_ARG     # workspace too small
+    assert call_host(lib, p, None, need) == binding.LA_ERR_INVALID_ARG       # no workspace
+    assert call_host(lib, p, fake(9, misalign=16), need) == binding.LA_ERR_MISALIGNED
+    assert call_host(lib, p, ws, need, dk=12) == binding.LA_ERR_UNSUPPORTED
+    q = list(p); q[4] = None                                                 # s0 without z0
+    assert call_host(lib, q, ws, need) == binding.LA_ERR_INVALID_ARG
+    q = list(p); q[5] = ctypes.c_void_p(p[0].value + 64)                     # y overlaps q
+    assert call_host(lib, q, ws, need) == binding.LA_ERR_INVALID_ARG
+    # host buffers need no alignment: a misaligned q still reaches the workspace check
+    q = list(p); q[0] = fake(0, misalign=2)
+    assert call_host(lib, q, ws, need - 1) == binding.LA_ERR_INVALID_ARG
