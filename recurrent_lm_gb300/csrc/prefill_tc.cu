@@ -160,9 +160,11 @@ __device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, i
 // Reads T at `tsrc` + 64 pp and writes the 32 packed bf16 columns to `tdst`,
 // which lie inside the columns this warp has just read.  Rows that see no key
 // of the block (2 pp > w) store zeros.
+// Kept out of line: the P warps and warps 2, 3 share one copy of this code
+// (the kernel's roles together run more code than the instruction cache holds).
 template <bool kPad, bool kDecay>
-__device__ __forceinline__ void p_block(uint32_t tsrc, uint32_t tdst, int pp, int i, int w, int kmin,
-                                        uint32_t pow) {
+static __device__ __noinline__ void p_block(uint32_t tsrc, uint32_t tdst, int pp, int i, int w, int kmin,
+                                            uint32_t pow) {
     uint32_t pw[32];
     if (2 * pp <= w) {
         const uint64_t c32 = f2pack(0.03125f, 0.03125f), c4 = f2pack(0.25f, 0.25f), c1 = f2pack(1.0f, 1.0f);
