@@ -57,7 +57,8 @@ constexpr int kNB = 80;          // B columns of the value side: 64 values + 16 
 
 // TMEM columns (512 allocated): S'^T|z' (160), num|den (80), two T = Q K^T
 // buffers (128 fp32 each); P (128 x 128 bf16, two per 32-bit column) is
-// written in place over the first 64 columns of its T.
+// written in place into its T: keys 0..63 over columns 0..31, keys 64..127
+// over columns 96..127.
 constexpr uint32_t kTmS = 0;
 constexpr uint32_t kTmNum = 160;
 __host__ __device__ constexpr uint32_t tm_t(int b) { return b ? 384u : 256u; }
