@@ -310,6 +310,16 @@ LA_API const char *la_status_string(la_status status);
  */
 LA_API la_status la_check_device_status(la_stream_t stream);
 
+/*
+ * la_debug_timeout_probe -- test aid for the failure path: enqueues on
+ * `stream` a one-thread kernel that waits, with the library's bounded wait,
+ * on a barrier that nothing completes.  After about one second the wait gives
+ * up, records a timeout in the device status word and the kernel returns (no
+ * trap, no fault; the context stays usable).  The next la_check_device_status
+ * returns LA_ERR_TIMEOUT.  Returns LA_ERR_CUDA if the launch failed.
+ */
+LA_API la_status la_debug_timeout_probe(la_stream_t stream);
+
 /* Library version as major*10000 + minor*100 + patch. */
 LA_API int la_version(void);
 

@@ -64,6 +64,7 @@ SIGNATURES = {
     "la_noalloc_scratch_bytes": (_SZ, []),
     "la_status_string": (ctypes.c_char_p, [_I]),
     "la_check_device_status": (_I, [_VP]),
+    "la_debug_timeout_probe": (_I, [_VP]),
     "la_version": (_I, []),
 }
 
@@ -355,6 +356,13 @@ def decode_step(q, k, v, s, z, *, eps: float = 0.0, y=None, s_out=None, z_out=No
                                         _ptr(s_out), _ptr(z_out), _ptr(y), B, H, dk, D_V, _dt(q),
                                         float(eps), _stream(stream)))
     return y, s_out, z_out
+
+
+def debug_timeout_probe(stream=None) -> None:
+    """Enqueue the bounded-wait failure probe (la_debug_timeout_probe): about one
+    second later the device status word holds a timeout, which the next
+    check_device_status raises as LAError(LA_ERR_TIMEOUT)."""
+    _raise(load_library().la_debug_timeout_probe(_stream(stream)))
 
 
 def check_device_status(stream=None) -> None:

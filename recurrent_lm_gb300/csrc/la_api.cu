@@ -486,6 +486,14 @@ la_status la_prefill_host(const void *q, const void *k, const void *v, const flo
     return result;
 }
 
+la_status la_debug_timeout_probe(la_stream_t stream) {
+    int dev;
+    unsigned *status;
+    la_status st = device_setup(&dev, &status);
+    if (st != LA_OK) return st;
+    return to_status(la::launch_timeout_probe(status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 la_status la_check_device_status(la_stream_t stream) {
     int dev;
     unsigned *status;

@@ -89,5 +89,6 @@ cudaError_t launch_prefix_partials_tc(const PrefixArgs &a, cudaStream_t st);
 cudaError_t launch_prefix_reduce(const PrefixArgs &a, cudaStream_t st);
 cudaError_t launch_state_copy(int64_t D, const float *s0, const float *z0, float *s_out,
                               float *z_out, int64_t BH, cudaStream_t st);
+cudaError_t launch_timeout_probe(unsigned *status, cudaStream_t st);
 
 }  // namespace la
