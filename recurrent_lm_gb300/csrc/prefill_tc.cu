@@ -171,25 +171,22 @@ static __device__ __noinline__ void p_block(uint32_t tsrc, uint32_t tdst, int pp
         const uint64_t c32 = f2pack(0.03125f, 0.03125f), c4 = f2pack(0.25f, 0.25f), c1 = f2pack(1.0f, 1.0f);
         const bool diag = 64 * pp + 63 >= 32 * w;  // this block reaches the diagonal
         if constexpr (kDecay) {
-            // in halves of 32 columns: the decay factors (gamma^(i-j), gamma^(i-j-1))
-            // from the power table need registers too; j > i is masked below
+            // times the decay factors (gamma^(i-j), gamma^(i-j-1)) from the power
+            // table; j > i is masked below
+            uint32_t r[64];
+            tmem_load64_sync(tsrc + 64 * pp, r);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t r[32];
-                tmem_load32_sync(tsrc + 64 * pp + 32 * h, r);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int key = 64 * pp + 32 * h + 2 * j;
-                    const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
-                    const uint64_t f2 = ld_shared_u64(pow + 8u * (uint32_t)max(i - key, 0));
-                    const uint64_t p2 = fmul2(ffma2(t2, ffma2(t2, c32, c4), c1), f2);
-                    float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
-                    if (diag) {
-                        if (key > i) p0 = 0.f;
-                        if (key + 1 > i) p1 = 0.f;
-                    }
-                    pw[16 * h + j] = pack_bf16(p0, p1);
+            for (int j = 0; j < 32; ++j) {
+                const int key = 64 * pp + 2 * j;
+                const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
+                const uint64_t f2 = ld_shared_u64(pow + 8u * (uint32_t)max(i - key, 0));
+                const uint64_t p2 = fmul2(ffma2(t2, ffma2(t2, c32, c4), c1), f2);
+                float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
+                if (diag) {
+                    if (key > i) p0 = 0.f;
+                    if (key + 1 > i) p1 = 0.f;
                 }
+                pw[j] = pack_bf16(p0, p1);
             }
         } else {
             uint32_t r[64];
