@@ -124,7 +124,9 @@ LA_API la_status la_prefill(const void *q, const void *k, const void *v,
  *
  * The call returns once the work is enqueued: the host outputs are valid
  * after `stream` has reached this point (cudaStreamSynchronize).  The inputs
- * must stay unchanged, and the outputs untouched, until then.
+ * must stay unchanged, and the outputs untouched, until then.  Not for use
+ * while `stream` is being captured into a CUDA graph (the call creates and
+ * destroys streams); la_prefill on device buffers is the capturable form.
  * d_feat 8/16/24/32 and both dtypes as la_prefill; no padding or decay.
  * Errors as la_prefill; a workspace that is too small is LA_ERR_INVALID_ARG.
  */
