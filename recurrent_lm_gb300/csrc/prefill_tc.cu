@@ -685,19 +685,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int i = 32 * w + lane;          // query row (num lane)
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
         // PV_READY(c) from the y warps: num drained after chunk c - 1, and (one
-        // lane) the loads P V(c) and Q K^T(c + 1) read, observed in order
-        auto pv_ready = [&](int c) -> bool {
-            if (tid == 384 && c < n &&
-                (!mbar_wait(bar(B_V_FULL + c % kStages), (uint32_t)(c / kStages) & 1u, abort, status) ||
-                 (c + 1 < n && !mbar_wait(bar(B_QK_FULL + (c + 1) % kStages), (uint32_t)((c + 1) / kStages) & 1u,
-                                          abort, status))))
-                return false;
-            if (lane == 0) mbar_arrive(bar(B_PV_READY));
-            return true;
+        // lane) the loads P V(c) and Q K^T(c + 1) read.  The lane observes those
+        // loads before it waits for the numerator (they have landed long before),
+        // so that the numerator drain alone sits on the path to the next P V.
+        auto observe = [&](int c) -> bool {
+            return tid != 384 || c >= n ||
+                   (mbar_wait(bar(B_V_FULL + c % kStages), (uint32_t)(c / kStages) & 1u, abort, status) &&
+                    (c + 1 >= n || mbar_wait(bar(B_QK_FULL + (c + 1) % kStages), (uint32_t)((c + 1) / kStages) & 1u,
+                                             abort, status)));
         };
-        bool ok = pv_ready(0);  // phase 0: num starts drained
+        bool ok = __all_sync(0xffffffffu, observe(0));
+        if (ok && lane == 0) mbar_arrive(bar(B_PV_READY));  // phase 0: num starts drained
         for (int c = 0; ok && c < n; ++c) {
             // ---- y(c)
+            const bool seen = observe(c + 1);
             if (!mbar_wait(bar(B_NUM_FULL), (uint32_t)c & 1u, abort, status)) break;
             if (tid == 384) LA_TR(TR_EPI, c, 2);
             __syncwarp();
@@ -707,7 +708,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tmem_load64_1_sync(tmem + lanebase + kTmNum, 64, r, dr);
                 tc_fence_before();
                 __syncwarp();
-                ok = __all_sync(0xffffffffu, pv_ready(c + 1));  // num of chunk c drained (warp-uniform result)
+                ok = __all_sync(0xffffffffu, seen);  // warp-uniform result
+                if (ok && lane == 0) mbar_arrive(bar(B_PV_READY));  // num of chunk c drained
                 // y rows of this warp -> its 4 KB staging tile -> one bulk tensor store
                 // (rows past N are clipped by the store)
                 float inv = 1.0f / (__uint_as_float(dr) + eps);
