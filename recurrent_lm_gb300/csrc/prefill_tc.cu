@@ -55,16 +55,23 @@ constexpr int kC = 128;          // tokens per chunk
 constexpr int kThreads = 512;
 constexpr int kNB = 80;          // B columns of the value side: 64 values + 16 normaliser
 
-// TMEM columns (512 allocated): S'^T|z' (160), num|den (80), two T = Q K^T
-// buffers (128 fp32 each); P (128 x 128 bf16, two per 32-bit column) is
-// written in place into its T: keys 0..63 over columns 0..31, keys 64..127
-// over columns 96..127.
+// TMEM columns (all 512): S'^T|z' (160), Phi'_Q (80: 160 bf16 features, two
+// per 32-bit column, the A operand of the read-out), num|den (80), T = Q K^T
+// (128 fp32) and P (64: 128 x 128 bf16, two keys per 32-bit column, the A
+// operand of P V).  Keeping Phi'_Q in TMEM rather than shared memory takes
+// 80 KB per chunk (its stores and the read-out's operand reads) off the
+// shared-memory data path, which the tensor core's other operand reads, the
+// TMA, the feature stores and every barrier operation share.  With P in its
+// own buffer, Q K^T of the next chunk may overwrite T as soon as the P warps
+// have read it.
 constexpr uint32_t kTmS = 0;
-constexpr uint32_t kTmNum = 160;
-__host__ __device__ constexpr uint32_t tm_t(int b) { return b ? 384u : 256u; }
+constexpr uint32_t kTmPhiQ = 160;
+constexpr uint32_t kTmNum = 240;
+constexpr uint32_t kTmT = 320;
+constexpr uint32_t kTmP = 448;
 
 // Shared memory map (bytes from a 1024-aligned base)
-constexpr uint32_t kSmPhiQ = 0;        // K-major A: [blk0 16K SW128][blk1 16K SW128][blk2 8K SW64]
+constexpr uint32_t kSmPhiQ = 0;        // 40 KB, free during the chunk loop (Phi'_Q lives in TMEM)
 constexpr uint32_t kSmPhiK = 40960;    // MN-major B: 3 x 16K SW128 (blk2: 32 of 64 features used)
 constexpr uint32_t kSmSb = 90112;      // K-major B [80 rows][160]: 2 x 10K SW128 + 5K SW64
 constexpr uint32_t kSmV = 116736;      // 3 x [128][64] bf16 SW128
@@ -81,7 +88,7 @@ constexpr int kStages = 3;
 // barrier indices
 enum {
     B_QK_FULL = 0, B_QK_EMPTY = 3, B_V_FULL = 6, B_V_EMPTY = 9,
-    B_T_FULL = 12,   // [2] per T buffer
+    B_T_FULL = 12,   // Q K^T of the chunk is in T
     // PV_READY(c): P(c) (P warps) and num drained after chunk c - 1 (y warps);
     // RO_READY(c): Phi'_Q(c) (gen warps) and the state operand after chunk c - 1
     // (conversion warps).  Merged so the MMA issuer waits once for each: its
@@ -156,18 +163,20 @@ __device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, i
 }
 
 // P = 1 + T/4 + T^2/32 for the keys 64 pp .. 64 pp + 63 of query row i (TMEM
-// lane quarter w), with the causal mask (key > i), left padding (key < kmin)
-// and, with decay, the factor gamma^(i - key) from the power table at `pow`.
-// Reads T at `tsrc` + 64 pp and writes the 32 packed bf16 columns to `tdst`,
-// which lie inside the columns this warp has just read.  Rows that see no key
-// of the block (2 pp > w) store zeros.
-// Kept out of line: the P warps and warps 2, 3 share one copy of this code
-// (the kernel's roles together run more code than the instruction cache holds).
+// lane quarter w, 2 pp <= w), with the causal mask (key > i), left padding
+// (key < kmin) and, with decay, the factor gamma^(i - key) from the power
+// table at `pow`.  Reads T at `tsrc` + 64 pp; once the previous chunk's P V
+// has read the P buffer (phase `wpar` of the barrier `wbar`; wbar = 0: no
+// wait) writes the 32 packed bf16 columns to `tdst`.  Returns false if that
+// wait gave up.  Kept out of line: the six P warps share one copy of this
+// code (the kernel's roles together run more code than the instruction cache
+// holds).
 template <bool kPad, bool kDecay>
-static __device__ __noinline__ void p_block(uint32_t tsrc, uint32_t tdst, int pp, int i, int w, int kmin,
-                                            uint32_t pow) {
+static __device__ __noinline__ bool p_block(uint32_t tsrc, uint32_t tdst, int pp, int i, int w, int kmin,
+                                            uint32_t pow, uint32_t wbar, uint32_t wpar, volatile int *abort,
+                                            unsigned *status) {
     uint32_t pw[32];
-    if (2 * pp <= w) {
+    {
         const uint64_t c32 = f2pack(0.03125f, 0.03125f), c4 = f2pack(0.25f, 0.25f), c1 = f2pack(1.0f, 1.0f);
         const bool diag = 64 * pp + 63 >= 32 * w;  // this block reaches the diagonal
         if constexpr (kDecay) {
@@ -212,11 +221,10 @@ static __device__ __noinline__ void p_block(uint32_t tsrc, uint32_t tdst, int pp
                 else if (key < kmin) pw[j] &= 0xFFFF0000u;  // low half = the even key
             }
         }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pw[j] = 0u;
     }
+    if (wbar && !__all_sync(0xffffffffu, mbar_wait(wbar, wpar, abort, status))) return false;
     tmem_store32_sync(tdst, pw);
+    return true;
 }
 
 // Image of one head's final [273][64] fp32 state in shared memory, written
@@ -286,9 +294,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_init(bar(B_V_FULL + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_T_FULL + i), 1);
-        }
+        mbar_init(bar(B_T_FULL), 1);
         mbar_init(bar(B_PV_READY), 6 + 4);  // P warps 8..11, 2, 3; y warps
         mbar_init(bar(B_RO_READY), 4 + 8);
         mbar_init(bar(B_PHK_FULL), 4);
@@ -441,8 +447,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // descriptor bases; per-step offsets are added in 16-byte units
             const uint64_t dQ = smem_desc(sb + kSmQ, 16, 256, kSw32);
             const uint64_t dK = smem_desc(sb + kSmK, 16, 256, kSw32);
-            const uint64_t dPhiQ = smem_desc(sb + kSmPhiQ, 16, 1024, kSw128);
-            const uint64_t dPhiQ2 = smem_desc(sb + kSmPhiQ + 32768, 16, 512, kSw64);
             const uint64_t dSb = smem_desc(sb + kSmSb, 16, 1024, kSw128);
             const uint64_t dSb2 = smem_desc(sb + kSmSb + 20480, 16, 512, kSw64);
             const uint64_t dPhiK = smem_desc(sb + kSmPhiK, 16384, 1024, kSw128);
@@ -452,10 +456,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             auto dVst = [&](int st) {
                 return dV0 + (uint64_t)(st * (16384 >> 4)) - ((uint64_t)(st * (16384 >> 4)) << 16);
             };
-            auto issue_qk = [&](int c) {  // T[c & 1] = Q_c K_c^T
+            auto issue_qk = [&](int c) {  // T = Q_c K_c^T
                 const int st = c % kStages;
-                mma_bf16_warp(tmem + tm_t(c & 1), dQ + st * (4096 >> 4), dK + st * (4096 >> 4), kIdQK, 0);
-                mma_commit_warp(bar(B_T_FULL + (c & 1)));  // also frees the q, k stage (P epilogue forwards it)
+                mma_bf16_warp(tmem + kTmT, dQ + st * (4096 >> 4), dK + st * (4096 >> 4), kIdQK, 0);
+                mma_commit_warp(bar(B_T_FULL));  // also frees the q, k stage (P epilogue forwards it)
             };
             bool ok = wwait(bar(B_QK_FULL + 0), 0);
             if (ok) {
@@ -463,13 +467,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 issue_qk(0);
             }
             for (int c = 0; ok && c < n; ++c) {
-                const int vs = c % kStages, b = c & 1;
+                const int vs = c % kStages;
                 const uint64_t dV = dVst(vs);
                 const uint32_t pc = (uint32_t)c & 1u;
-                // P(c) is in T[b]; V(c) is in; num was drained for chunk c - 1 (which
-                // also means P V of chunk c - 1 completed: the read-out commit covers
-                // every earlier MMA, so T[b ^ 1] may take Q K^T(c + 1)); q, k of c + 1
-                // (PV_READY(c) also covers V(c) and q, k of chunk c + 1: a y warp
+                // P(c) is in the P buffer (so the P warps have read T, which may take
+                // Q K^T(c + 1)); V(c) is in; num was drained for chunk c - 1; q, k of
+                // c + 1 (PV_READY(c) also covers V(c) and q, k of chunk c + 1: a y warp
                 // observes those loads before it arrives, sparing this thread the waits)
                 ok = wwait(bar(B_PV_READY), pc);
                 if (!ok) break;
@@ -477,27 +480,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 tc_fence_after();
                 if (c + 1 < n) issue_qk(c + 1);
                 if (lane == 0) LA_TR(TR_MMA, c, 1);
-                // intra-chunk: [num | den] = P [V | 1], P from TMEM
+                // intra-chunk: [num | den] = P [V | 1], P from TMEM (keys 16 s.. in
+                // packed columns 8 s..)
 #pragma unroll
-                for (int s = 0; s < 8; ++s)  // keys 16 s..: packed columns 8 s (s < 4), 64 + 8 s (s >= 4)
-                    mma_bf16_ts_warp(tmem + kTmNum, tmem + tm_t(b) + 8 * s + (s >= 4 ? 64 : 0),
-                                     dV + s * (2048 >> 4), kIdPV, s > 0);
+                for (int s = 0; s < 8; ++s)
+                    mma_bf16_ts_warp(tmem + kTmNum, tmem + kTmP + 8 * s, dV + s * (2048 >> 4), kIdPV, s > 0);
                 // inter-chunk read-out operands: the state after chunk c - 1, Phi'_Q(c)
                 ok = wwait(bar(B_RO_READY), pc);
                 if (!ok) break;
                 if (lane == 0) LA_TR(TR_MMA, c, 2);
                 tc_fence_after();
-                // inter-chunk read-out: [num | den] += Phi'_Q [S' | z'] (both K-major)
+                // inter-chunk read-out: [num | den] += Phi'_Q [S' | z'], Phi'_Q from TMEM
+                // (features 16 s.. in columns 8 s..), the state K-major in shared memory
 #pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t o = (uint32_t)((s >> 2) * 16384 + (s & 3) * 32) >> 4;
-                    const uint32_t ob = (uint32_t)((s >> 2) * 10240 + (s & 3) * 32) >> 4;
-                    mma_bf16_warp(tmem + kTmNum, dPhiQ + o, dSb + ob, kIdRO, 1);
+                for (int s = 0; s < 10; ++s) {
+                    const uint64_t db = s < 8 ? dSb + ((uint32_t)((s >> 2) * 10240 + (s & 3) * 32) >> 4)
+                                              : dSb2 + ((uint32_t)((s - 8) * 32) >> 4);
+                    mma_bf16_ts_warp(tmem + kTmNum, tmem + kTmPhiQ + 8 * s, db, kIdRO, 1);
                 }
-#pragma unroll
-                for (int s = 8; s < 10; ++s)
-                    mma_bf16_warp(tmem + kTmNum, dPhiQ2 + ((s - 8) * 32 >> 4), dSb2 + ((s - 8) * 32 >> 4), kIdRO, 1);
-                mma_commit_warp(bar(B_NUM_FULL));  // also: Phi'_Q buffer free
+                mma_commit_warp(bar(B_NUM_FULL));  // also: Phi'_Q and the P buffer free
                 // state update operand Phi'_K(c)
                 if (!(ok = wwait(bar(B_PHK_FULL), pc))) break;
                 if (lane == 0) LA_TR(TR_MMA, c, 3);
@@ -522,12 +523,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
         const int kmin = kPad ? lpad : 0;
         for (int c = 0; c < n; ++c) {
-            const int b = c & 1;
-            if (!mbar_wait(bar(B_T_FULL + b), (uint32_t)(c >> 1) & 1u, abort, status)) break;
-            __syncwarp();  // tcgen05.ld/st below are warp-collective (.sync.aligned)
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_T_FULL), (uint32_t)c & 1u, abort, status))) break;
             tc_fence_after();
-            const uint32_t tb = tmem + lanebase + tm_t(b);
-            p_block<kPad, kDecay>(tb, tb + 96, 1, i, w, kmin - c * kC, sb + kSmPow);
+            // P V of chunk c - 1 completed with the read-out (NUM_FULL(c - 1))
+            if (!p_block<kPad, kDecay>(tmem + lanebase + kTmT, tmem + lanebase + kTmP + 32, 1, i, w, kmin - c * kC,
+                                       sb + kSmPow, c > 0 ? bar(B_NUM_FULL) : 0u, (uint32_t)(c - 1) & 1u, abort,
+                                       status))
+                break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PV_READY));
@@ -551,16 +553,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             load_row16_raw(sb + kSmK + st * 4096, t, klo, khi);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_QK_EMPTY + st));
-            // the read-out of chunk c - 1 (NUM_FULL) released the Phi'_Q buffer
-            if (!mbar_wait(bar(B_NUM_FULL), pc ^ 1u, abort, status)) break;
+            // the read-out of chunk c - 1 (NUM_FULL) released Phi'_Q; it goes into this
+            // thread's TMEM lane (token t), the read-out's A operand
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_NUM_FULL), pc ^ 1u, abort, status))) break;
+            tc_fence_after();
             if constexpr (kDecay) {  // token t reads gamma^(t+1) of the state before the chunk
                 const float lq = pow_gamma(t + 1);
-                emit_features<false, true>(qlo, qhi, sb + kSmPhiQ, t, false, std::make_integer_sequence<int, 20>{},
-                                           pack_bf16(lq, lq));
+                emit_features_tmem<false, true>(qlo, qhi, tmem + lanebase + kTmPhiQ,
+                                                std::make_integer_sequence<int, 5>{}, pack_bf16(lq, lq));
             } else {
-                emit_features<false>(qlo, qhi, sb + kSmPhiQ, t, false, std::make_integer_sequence<int, 20>{});
+                emit_features_tmem<false>(qlo, qhi, tmem + lanebase + kTmPhiQ, std::make_integer_sequence<int, 5>{});
             }
-            fence_async_smem();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_RO_READY));
             if (tid == 128) LA_TR(TR_GEN, c, 1);
@@ -623,20 +627,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int i = tid - 256;  // query row within the chunk (= TMEM lane)
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
         const bool zrow = (w == 2);  // warp 10: lane 64 holds z'
+        // rows 0..63 see no key of 64..127: their P columns 32..63 stay zero
+        if (w < 2) {
+            uint32_t zero[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) zero[j] = 0u;
+            tmem_store32_sync(tmem + lanebase + kTmP + 32, zero);
+        }
         auto do_p = [&](int c) -> bool {
-            const int b = c & 1;
-            if (!mbar_wait(bar(B_T_FULL + b), (uint32_t)(c >> 1) & 1u, abort, status)) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_T_FULL), (uint32_t)c & 1u, abort, status))) return false;
             if (tid == 256) mbar_arrive(bar(B_QK_EMPTY + c % kStages));  // Q K^T(c) has read its q, k stage
             if (tid == 256 + 96) LA_TR(TR_EPI, c, 0);
-            __syncwarp();  // tcgen05.ld/st below are warp-collective (.sync.aligned)
             tc_fence_after();
-            const uint32_t tb = tmem + lanebase + tm_t(b);
             const int kmin = kPad ? lpad - c * kC : 0;  // keys below kmin are left padding
-            // keys 0..63 -> packed columns 0..31 of T; keys 64..127 (packed columns
-            // 96..127) of lane quarters 2, 3 are warps 2, 3's share, and rows below
-            // 64 see none of them
-            p_block<kPad, kDecay>(tb, tb, 0, i, w, kmin, sb + kSmPow);
-            if (w < 2) p_block<kPad, kDecay>(tb, tb + 96, 1, i, w, kmin, sb + kSmPow);
+            // keys 0..63 -> P columns 0..31; keys 64..127 of lane quarters 2, 3 are
+            // warps 2, 3's share (P columns 32..63).  The store waits until P V of
+            // chunk c - 1 has completed (NUM_FULL(c - 1)).
+            if (!p_block<kPad, kDecay>(tmem + lanebase + kTmT, tmem + lanebase + kTmP, 0, i, w, kmin, sb + kSmPow,
+                                       c > 0 ? bar(B_NUM_FULL) : 0u, (uint32_t)(c - 1) & 1u, abort, status))
+                return false;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PV_READY));

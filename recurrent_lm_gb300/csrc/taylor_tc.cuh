@@ -142,6 +142,43 @@ __device__ __forceinline__ void emit_features(const uint4 &lo, const uint4 &hi, 
     }
 }
 
+// Feature vector of one token into its TMEM lane (columns taddr + r for the
+// 80 packed pairs r, the layout of an A operand in TMEM: two consecutive K
+// elements per 32-bit column), with 5 warp-collective stores of 16 columns.
+template <bool kKey, int G, int... J>
+__device__ __forceinline__ void store_feature_group(const uint32_t (&XL)[8], const uint32_t (&X)[8],
+                                                    const uint32_t (&Y)[7], const uint32_t (&H)[8],
+                                                    uint32_t b15, uint32_t cst, uint32_t taddr,
+                                                    std::integer_sequence<int, J...>) {
+    uint32_t w[16];
+    ((w[J] = feat_pair<kKey, 16 * G + J>(XL, X, Y, H, b15, cst)), ...);
+    tmem_store16_sync(taddr + 16 * G, w);
+}
+template <bool kKey, bool kScaled = false, int... G>
+__device__ __forceinline__ void emit_features_tmem(const uint4 &lo, const uint4 &hi, uint32_t taddr,
+                                                   std::integer_sequence<int, G...>,
+                                                   uint32_t scale2 = 0x3F803F80u) {
+    const uint32_t raw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t X[8], Y[7], H[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) X[j] = hmul2(raw[j], 0x3F003F00u);
+#pragma unroll
+    for (int j = 0; j < 7; ++j) Y[j] = __byte_perm(X[j], X[j + 1], 0x5432);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) H[j] = kKey ? hmul2(X[j], 0x3F003F00u) : 0u;
+    const uint32_t b15 = __byte_perm(X[7], X[7], 0x3232);
+    if constexpr (kScaled) {
+        uint32_t XL[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) XL[j] = hmul2(X[j], scale2);
+        (store_feature_group<kKey, G>(XL, X, Y, H, b15, scale2 & 0xFFFFu, taddr,
+                                      std::make_integer_sequence<int, 16>{}), ...);
+    } else {
+        (store_feature_group<kKey, G>(X, X, Y, H, b15, 0x00003F80u, taddr,
+                                      std::make_integer_sequence<int, 16>{}), ...);
+    }
+}
+
 // Raw token row t (16 bf16 as two 16-byte halves) of a [128][16] SW32 tile.
 __device__ __forceinline__ void load_row16_raw(uint32_t tile, int t, uint4 &lo, uint4 &hi) {
     const uint32_t sw = (uint32_t)((t >> 2) & 1);
