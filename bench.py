@@ -573,7 +573,8 @@ def main():
     head_tokens = pre["B"] * pre["H"] * pre["N"]
     s_ = pre["ms"] / 1e3
     flops = head_tokens * FLOPS_PER_HEAD_TOKEN
-    nbytes = head_tokens * BYTES_PER_HEAD_TOKEN_BF16 + 3 * pre["B"] * pre["H"] * STATE_BYTES
+    # s0, z0 read once and s, z written once per head (STATE_BYTES covers s and z)
+    nbytes = head_tokens * BYTES_PER_HEAD_TOKEN_BF16 + 2 * pre["B"] * pre["H"] * STATE_BYTES
     achieved_tf = flops / s_ / 1e12
     hbm_gbs = nbytes / s_ / 1e9
     traffic = kernel_traffic("prefill")

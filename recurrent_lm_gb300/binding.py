@@ -128,6 +128,14 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _keep_for(t: torch.Tensor, stream):
+    """A tensor allocated here (on the current stream) but used by work
+    enqueued on another stream: tell the caching allocator, so that the block
+    is not handed out again before that stream's work has finished with it."""
+    if stream is not None and stream != torch.cuda.current_stream(t.device):
+        t.record_stream(stream)
+
+
 def _need_pad(left_pad, B):
     if left_pad is not None:
         _need(left_pad, "left_pad", (B,), torch.int32)
@@ -235,10 +243,13 @@ def prefill_host(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=N
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
         need = prefill_host_workspace_size(B, H, N, dk, dt)
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        _keep_for(workspace, stream)
     _need(workspace, "workspace", (workspace.numel(),), torch.uint8)
-    _raise(lib.la_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
-                               _ptr(z_out), _ptr(workspace), workspace.numel(), B, H, N, dk, D_V,
-                               _dt(q), float(eps), _stream(stream)))
+    # the library works on the current device: make it the workspace's
+    with torch.cuda.device(workspace.device):
+        _raise(lib.la_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
+                                   _ptr(z_out), _ptr(workspace), workspace.numel(), B, H, N, dk, D_V,
+                                   _dt(q), float(eps), _stream(stream)))
     return y, s_out, z_out
 
 
@@ -276,6 +287,7 @@ def prefix_prefill(q, k, v, k_e, v_e, s0=None, z0=None, *, eps: float = 0.0, y=N
     need = prefix_workspace_size(B, H, M)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        _keep_for(workspace, stream)
     _need_pad(left_pad, B)
     if left_pad is None:
         _raise(lib.la_prefix_prefill(

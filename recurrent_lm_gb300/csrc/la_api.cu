@@ -417,9 +417,11 @@ la_status la_prefill_host(const void *q, const void *k, const void *v, const flo
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LA_ERR_MISALIGNED;
     const Range in[] = {{q, es * BH * N * d_feat}, {k, es * BH * N * d_feat}, {v, es * BH * N * kDV},
                         {s0, sizeof(float) * BH * D * kDV}, {z0, sizeof(float) * BH * D}};
+    // the workspace is written by the call too: no input or output may overlap it
     const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * D * kDV},
-                         {z_out, sizeof(float) * BH * D}};
-    if (any_overlap(in, 5, out, 3)) return LA_ERR_INVALID_ARG;
+                         {z_out, sizeof(float) * BH * D},
+                         {workspace, host_workspace_bytes(BH, N, d_feat, es)}};
+    if (any_overlap(in, 5, out, 4)) return LA_ERR_INVALID_ARG;
     int dev;
     unsigned *status;
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;

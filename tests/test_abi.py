@@ -226,3 +226,7 @@ def test_host_prefill_rejects_bad_args(lib):
     # host buffers need no alignment: a misaligned q still reaches the workspace check
     q = list(p); q[0] = fake(0, misalign=2)
     assert call_host(lib, q, ws, need - 1) == binding.LA_ERR_INVALID_ARG
+    # the workspace must not overlap an input or an output (device-resident
+    # buffers are accepted, so they could)
+    assert call_host(lib, p, ctypes.c_void_p(p[0].value + 256), need) == binding.LA_ERR_INVALID_ARG
+    assert call_host(lib, p, ctypes.c_void_p(p[6].value), need) == binding.LA_ERR_INVALID_ARG

@@ -103,6 +103,46 @@ def test_decode_full_batch_sampled_heads():
     assert_close("z", zs, z_r, TOL[torch.bfloat16])
 
 
+def test_decode_graph_pipeline_full_batch():
+    """The benchmark's decode pipeline: B=128, H=16, the state from a 2048-token
+    GPU prefill, then T=128 consecutive in-place decode steps captured in one
+    CUDA graph and replayed.  Every step's y and the final state of 8 sampled
+    heads against the oracle run from the same initial state."""
+    w = inputs.WORKLOADS[5]
+    B, H, T = w.B, w.H, 128
+    qs, ks, vs = inputs.s0_sequence(5)
+    _, s, z = la.prefill(qs.to(DEV), ks.to(DEV), vs.to(DEV))
+    torch.cuda.synchronize()
+    heads = sample_heads(B, H, 8, seed=6)
+    s_r = torch.stack([s[b, h] for b, h in heads])[None].double().cpu().numpy()
+    z_r = torch.stack([z[b, h] for b, h in heads])[None].double().cpu().numpy()
+    steps = [inputs.decode_step_inputs(5, i) for i in range(T)]
+    qd = torch.stack([t[0] for t in steps]).to(DEV)
+    kd = torch.stack([t[1] for t in steps]).to(DEV)
+    vd = torch.stack([t[2] for t in steps]).to(DEV)
+    yd = torch.empty((T, B, H, 64), dtype=torch.bfloat16, device=DEV)
+    # one call before capture (per-device set-up), on a copy of the state
+    la.decode_step(qd[0], kd[0], vd[0], s.clone(), z.clone(), y=yd[0], inplace=True)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(T):
+                la.decode_step(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True)
+    graph.replay()
+    torch.cuda.synchronize()
+    la.check_device_status()
+    tol = TOL[torch.bfloat16]
+    for i, (q, k, v) in enumerate(steps):
+        qq, kk, vv = (torch.stack([t[b, h] for b, h in heads])[None] for t in (q, k, v))
+        y_r, s_r, z_r = oracle.decode_step(qq, kk, vv, s_r, z_r)
+        assert_close(f"y step {i}", torch.stack([yd[i, b, h] for b, h in heads])[None], y_r, tol)
+    assert_close("s", torch.stack([s[b, h] for b, h in heads])[None], s_r, tol)
+    assert_close("z", torch.stack([z[b, h] for b, h in heads])[None], z_r, tol)
+
+
 # ------------------------------------------------------------------ prefix
 def run_prefix(q, k, v, ke, ve, s0=None, z0=None):
     dev = [t.to(DEV) if t is not None else None for t in (q, k, v, ke, ve, s0, z0)]

@@ -97,3 +97,24 @@ def test_host_rejects_small_workspace():
     with pytest.raises(la.LAError) as e:
         la.prefill_host(*pinned(q, k, v), workspace=ws)
     assert e.value.status == la.LA_ERR_INVALID_ARG
+
+
+def test_host_prefill_on_a_side_stream():
+    """The workspace allocated by the binding is used on the caller's stream,
+    not the current one: with other allocations and work on the current
+    stream meanwhile, the side-stream call still matches the device path."""
+    q, k, v, _, _ = inputs.qkv(4, 4, 700, seed=905, dtype=torch.bfloat16)
+    s0, z0 = inputs.random_state(4, 4, seed=906)
+    ref = device_run(q, k, v, s0, z0)
+    side = torch.cuda.Stream()
+    hq, hk, hv, hs0, hz0 = pinned(q, k, v, s0, z0)
+    outs = []
+    for _ in range(3):
+        outs.append(la.prefill_host(hq, hk, hv, hs0, hz0, stream=side))
+        # current-stream work that would reuse a freed workspace block
+        junk = torch.full((1 << 22,), 7, dtype=torch.uint8, device=DEV)
+        junk.add_(1)
+    side.synchronize()
+    torch.cuda.synchronize()
+    for y, s, z in outs:
+        assert torch.equal(y, ref[0]) and torch.equal(s, ref[1]) and torch.equal(z, ref[2])
