@@ -55,6 +55,7 @@ FLOPS_PER_PREFIX_TOKEN = 35490      # update only
 BYTES_PER_HEAD_TOKEN_BF16 = 320     # q 32 + k 32 + v 128 + y 128
 BYTES_PER_PREFIX_TOKEN_BF16 = 160   # k_e 32 + v_e 128
 STATE_BYTES = 273 * 64 * 4 + 273 * 4  # one head's s and z (fp32)
+COMPACT_STATE_BYTES = 153 * 64 * 4 + 153 * 4  # the same in the 153-row compact layout
 
 
 def log(*a):
@@ -421,8 +422,10 @@ def leg_general_dk(la, args, dist, dev):
     return out
 
 
-def leg_decode(la, args, dist, dev, decay: bool = False):
-    """512 decode steps in one CUDA graph (with decay: la_decode_step_decay)."""
+def leg_decode(la, args, dist, dev, decay: bool = False, compact: bool = False):
+    """512 decode steps in one CUDA graph (with decay: la_decode_step_decay;
+    compact: the 153-row state from la_prefill_compact and
+    la_decode_step_compact)."""
     w = inputs.WORKLOADS[5]
     B, H, T = w.B, w.H, args.decode_steps
     g = torch.Generator(device=dev)
@@ -430,15 +433,21 @@ def leg_decode(la, args, dist, dev, decay: bool = False):
     qs = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
     ks = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
     vs = gen_device((B, H, w.s0_tokens, 64), g, dev=dev)
-    _, s, z = la.prefill(qs, ks, vs)
+    _, s, z = (la.prefill_compact if compact else la.prefill)(qs, ks, vs)
     del qs, ks, vs
     qd = gen_device((T, B, H, 16), g, dev=dev)
     kd = gen_device((T, B, H, 16), g, dev=dev)
     vd = gen_device((T, B, H, 64), g, dev=dev)
     yd = torch.empty((T, B, H, 64), dtype=torch.bfloat16, device=dev)
     gam = decay_rates(H, dev) if decay else None
+
+    def one(i):
+        if compact:
+            la.decode_step_compact(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True)
+        else:
+            la.decode_step(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True, gamma=gam)
     # warm up the library (per-device set-up) before capture
-    la.decode_step(qd[0], kd[0], vd[0], s, z, y=yd[0], inplace=True, gamma=gam)
+    one(0)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
@@ -446,7 +455,7 @@ def leg_decode(la, args, dist, dev, decay: bool = False):
     with torch.cuda.stream(cap):
         with torch.cuda.graph(graph, stream=cap):
             for i in range(T):
-                la.decode_step(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True, gamma=gam)
+                one(i)
     torch.cuda.synchronize()
     ms = time_loop(graph.replay, max(1, args.steps // 4), max(3, args.warmup // 2), dist)
     la.check_device_status()
@@ -475,8 +484,10 @@ def ncu_case(la, case: str):
     """Small launches for ncu captures (a few GB on the device at most, inputs
     still larger than L2): prefill B=16, H=16 at N=4096 then N=8192 with an
     initial state, two launches each (DRAM traffic is linear in N, so the
-    full-length launch is extrapolated from the two sizes); decode at the bench
-    batch B=128, H=16, four steps in place; prefix N=M=4096, three calls."""
+    full-length launch is extrapolated from the two sizes); decode (273-row or
+    compact state) at the bench batch B=128, H=16, ten steps in place back to
+    back (inputs generated first, so that nothing runs between the steps);
+    prefix N=M=4096, three calls."""
     dev = "cuda:0"
     g = torch.Generator(device=dev)
     g.manual_seed(0)
@@ -492,15 +503,19 @@ def ncu_case(la, case: str):
                 la.prefill(q, k, v, s0, z0)
             torch.cuda.synchronize()
             del q, k, v
-    elif case == "decode":
-        B, H = 128, 16
-        s = torch.randn(B, H, 273, 64, device=dev, generator=g)
-        z = torch.rand(B, H, 273, device=dev, generator=g) + 100.0
-        for _ in range(4):
-            q = gen_device((B, H, 16), g, dev=dev)
-            k = gen_device((B, H, 16), g, dev=dev)
-            v = gen_device((B, H, 64), g, dev=dev)
-            la.decode_step(q, k, v, s, z, inplace=True)
+    elif case in ("decode", "decode_compact"):
+        B, H, T = 128, 16, 10
+        D = 153 if case == "decode_compact" else 273
+        s = torch.randn(B, H, D, 64, device=dev, generator=g)
+        z = torch.rand(B, H, D, device=dev, generator=g) + 100.0
+        q = gen_device((T, B, H, 16), g, dev=dev)
+        k = gen_device((T, B, H, 16), g, dev=dev)
+        v = gen_device((T, B, H, 64), g, dev=dev)
+        y = torch.empty((T, B, H, 64), dtype=torch.bfloat16, device=dev)
+        step = la.decode_step_compact if case == "decode_compact" else la.decode_step
+        torch.cuda.synchronize()
+        for i in range(T):
+            step(q[i], k[i], v[i], s, z, y=y[i], inplace=True)
     elif case == "prefix":
         B, H, N, M = 16, 16, 4096, 4096
         q, k = gen_device((B, H, N, 16), g, dev=dev), gen_device((B, H, N, 16), g, dev=dev)
@@ -523,12 +538,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs",
-                    default="prefill,prefix,prefix_padded,jrt_prompt,prefill_decay,general_dk,decode,decode_decay")
+                    default="prefill,prefix,prefix_padded,jrt_prompt,prefill_decay,general_dk,decode,"
+                            "decode_decay,decode_compact")
     ap.add_argument("--decode-steps", type=int, default=512)
     ap.add_argument("--cpu-sample-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode", "prefix"],
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_compact", "prefix"],
                     help="run one small case for an ncu capture and exit (no timing)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -566,6 +582,8 @@ def main():
         res["decode"] = leg_decode(la, args, dist, dev)
     if "decode_decay" in legs:
         res["decode_decay"] = leg_decode(la, args, dist, dev, decay=True)
+    if "decode_compact" in legs:
+        res["decode_compact"] = leg_decode(la, args, dist, dev, compact=True)
     pre["clocks"] = clocks.stop()
 
     W = dist.world
@@ -662,21 +680,23 @@ def main():
                 "ms_per_call": r["ms"], "tokens_per_s": W * r["B"] * r["N"] / t,
                 "achieved_tflops": fl / t / 1e12, "path": "CUDA cores (general d')"}
             launches += max(1, args.steps // 20)
-    for dname in ("decode", "decode_decay"):
+    suffix = {"decode": "", "decode_decay": "-decay-1-2^-(4+h)", "decode_compact": "-compact-state-153"}
+    for dname in ("decode", "decode_decay", "decode_compact"):
         if dname not in res:
             continue
         r = res[dname]
         per_step_ms = r["ms_per_graph"] / r["steps_per_graph"]
         bh = r["B"] * r["H"]
-        by = bh * (2 * STATE_BYTES + BYTES_PER_HEAD_TOKEN_BF16)
+        sbytes = COMPACT_STATE_BYTES if dname == "decode_compact" else STATE_BYTES
+        by = bh * (2 * sbytes + BYTES_PER_HEAD_TOKEN_BF16)
         gbs = by / (per_step_ms / 1e3) / 1e9
         line["legs"][dname] = {
-            "workload": inputs.WORKLOADS[5].name + ("-decay-1-2^-(4+h)" if dname == "decode_decay" else ""),
+            "workload": inputs.WORKLOADS[5].name + suffix[dname],
             "us_per_step": per_step_ms * 1e3,
             "tokens_per_s": W * r["B"] / (per_step_ms / 1e3),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / pk["hbm_gbs"],
-                         "traffic": kernel_traffic("decode") if dname == "decode" else None,
+                         "traffic": kernel_traffic(dname) if dname != "decode_decay" else None,
                          "algorithmic_bytes_per_launch": by},
             "cuda_graph_steps": r["steps_per_graph"], "finite": r["finite"]}
         launches += r["steps_per_graph"] * max(1, args.steps // 4)

@@ -264,6 +264,90 @@ LA_API la_status la_decode_step(const void *q, const void *k, const void *v,
                          la_dtype dtype, float eps, la_stream_t stream);
 
 /*
+ * Compact state layout (d_feat = 16 only).
+ *
+ * The BASED reading notes (sec. 2.3) observe that vec(xbar xbar^T) holds each
+ * product xbar_a xbar_b (a != b) twice, so the same kernel
+ *   phi(q)^T phi(k) = 1 + q.k/4 + (q.k)^2/32
+ * is reached with 1 + d' + d'(d'+1)/2 = 153 features: the squares scaled by
+ * 1/sqrt(2) and each cross term once, unscaled:
+ *
+ *   phi_c(x) = [1, xbar_a (a = 0..15), xbar_a^2 / sqrt(2) (a = b), xbar_a xbar_b (a < b)]
+ *
+ * Sec. 2.5 notes that decoding reads and writes the whole state every step;
+ * the compact state is 153 rows instead of 273 (1.78x fewer bytes).
+ *
+ *   s_c [B][H][153][64] fp32,  z_c [B][H][153] fp32
+ *   row 0: constant; row 1 + a: linear xbar_a;
+ *   row 17 + c(a, b), a <= b: quadratic, c(a, b) = 16 a - a (a - 1) / 2 + (b - a)
+ *   (row-major over the upper triangle: (0,0) is row 17, (0,15) row 32,
+ *   (1,1) row 33, (15,15) row 152).
+ *
+ * Relation to the 273-row state s: s_c[0] = s[0], s_c[1 + a] = s[1 + a],
+ *   s_c[17 + c(a, a)] = s[17 + 17 a],
+ *   s_c[17 + c(a, b)] = (s[17 + 16 a + b] + s[17 + 16 b + a]) / sqrt(2)  (a < b),
+ * and the same for z.  Only the symmetric part of the 273-row quadratic
+ * block survives: the antisymmetric part (s[ab] - s[ba]) / 2 is DROPPED by
+ * the conversion.  It is zero in every state the recurrence builds (phi(k)
+ * is symmetric in (a, b)) and no output ever reads it (phi(q) is symmetric
+ * too), so y and every later compact state are unaffected; only a 273-row
+ * state that was set by hand with an antisymmetric part does not come back
+ * from a round trip.  From compact to 273 rows, the cross term is split
+ * evenly: s[ab] = s[ba] = s_c[17 + c(a, b)] / sqrt(2).
+ *
+ * All compact entry points take d_feat = 16 and d_v = 64 only
+ * (LA_ERR_UNSUPPORTED else); pointers, alignment (16 bytes), overlap and
+ * stream rules are the common ones above.
+ */
+#define LA_D_COMPACT 153   /* 1 + 16 + 16*17/2 */
+
+/*
+ * la_state_to_compact / la_state_from_compact -- convert B*H states between
+ * the 273-row and the compact layout (formulas above).
+ *   s  [B][H][273][64], z  [B][H][273] fp32 (DEVICE)
+ *   s_c [B][H][153][64], z_c [B][H][153] fp32 (DEVICE)
+ * Every pointer is required; input and output must not overlap.
+ */
+LA_API la_status la_state_to_compact(const float *s, const float *z, float *s_c, float *z_c,
+                                     int64_t B, int64_t H, int d_feat, int d_v,
+                                     la_stream_t stream);
+LA_API la_status la_state_from_compact(const float *s_c, const float *z_c, float *s, float *z,
+                                       int64_t B, int64_t H, int d_feat, int d_v,
+                                       la_stream_t stream);
+
+/*
+ * la_prefill_compact -- la_prefill with the initial and final states in the
+ * compact layout: s0_c / z0_c [B][H][153][64] / [B][H][153] fp32 or NULL (both
+ * or neither; NULL = zero state), s_out_c / z_out_c likewise or NULL.  y is
+ * the same as la_prefill's on the unfolded state (the dropped antisymmetric
+ * part is invisible to it).  dtype LA_DTYPE_BF16 only (the tensor-core path,
+ * whose internal state is already this 153-feature form); LA_DTYPE_F32 is
+ * LA_ERR_UNSUPPORTED (use la_prefill and la_state_to_compact).  Other
+ * arguments and errors as la_prefill.
+ */
+LA_API la_status la_prefill_compact(const void *q, const void *k, const void *v,
+                                    const float *s0_c, const float *z0_c,
+                                    void *y, float *s_out_c, float *z_out_c,
+                                    int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                                    la_dtype dtype, float eps, la_stream_t stream);
+
+/*
+ * la_decode_step_compact -- la_decode_step on a compact state: with
+ * phi_c as above, s_c += phi_c(k) v^T, z_c += phi_c(k), then
+ * y = phi_c(q)^T s_c / (phi_c(q)^T z_c + eps).
+ *   q, k [B][H][16], v [B][H][64] dtype (bf16 or fp32)
+ *   s_in_c, z_in_c, s_out_c, z_out_c: compact layout, all required;
+ *   s_out_c == s_in_c and z_out_c == z_in_c exactly is the in-place update.
+ *   y [B][H][64] dtype.
+ * Errors as la_decode_step.
+ */
+LA_API la_status la_decode_step_compact(const void *q, const void *k, const void *v,
+                                        const float *s_in_c, const float *z_in_c,
+                                        float *s_out_c, float *z_out_c, void *y,
+                                        int64_t B, int64_t H, int d_feat, int d_v,
+                                        la_dtype dtype, float eps, la_stream_t stream);
+
+/*
  * la_prefix_prefill_noalloc -- the same computation as la_prefix_prefill, for
  * callers that cannot allocate device memory when they call (for example a
  * serving loop that must not trigger the device synchronisation an

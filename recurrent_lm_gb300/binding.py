@@ -17,6 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblinattn.so")
 D_FEAT, D_V, D_PHI = 16, 64, 273
+D_COMPACT = 153  # rows of the compact state layout (1 + 16 + 16*17/2)
 
 
 def feature_dim(dk: int) -> int:
@@ -62,6 +63,12 @@ SIGNATURES = {
     "la_prefix_prefill_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _FP, _FP,
                                        _I64, _I64, _I64, _I, _I, _I, _F, _VP]),
     "la_noalloc_scratch_bytes": (_SZ, []),
+    "la_state_to_compact": (_I, [_FP, _FP, _FP, _FP, _I64, _I64, _I, _I, _VP]),
+    "la_state_from_compact": (_I, [_FP, _FP, _FP, _FP, _I64, _I64, _I, _I, _VP]),
+    "la_prefill_compact": (_I, [_VP, _VP, _VP, _FP, _FP, _VP, _FP, _FP, _I64, _I64, _I64, _I, _I,
+                                _I, _F, _VP]),
+    "la_decode_step_compact": (_I, [_VP, _VP, _VP, _FP, _FP, _FP, _FP, _VP, _I64, _I64, _I, _I, _I,
+                                    _F, _VP]),
     "la_status_string": (ctypes.c_char_p, [_I]),
     "la_check_device_status": (_I, [_VP]),
     "la_debug_timeout_probe": (_I, [_VP]),
@@ -367,6 +374,100 @@ def decode_step(q, k, v, s, z, *, eps: float = 0.0, y=None, s_out=None, z_out=No
         _raise(lib.la_decode_step_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(s), _ptr(z),
                                         _ptr(s_out), _ptr(z_out), _ptr(y), B, H, dk, D_V, _dt(q),
                                         float(eps), _stream(stream)))
+    return y, s_out, z_out
+
+
+def state_to_compact(s, z, *, s_c=None, z_c=None, stream=None):
+    """la_state_to_compact: s [B,H,273,64], z [B,H,273] fp32 -> the compact
+    layout s_c [B,H,153,64], z_c [B,H,153] (the antisymmetric part of the
+    quadratic block is dropped)."""
+    lib = load_library()
+    B, H = s.shape[:2]
+    _need(s, "s", (B, H, D_PHI, D_V), torch.float32)
+    _need(z, "z", (B, H, D_PHI), torch.float32)
+    if s_c is None:
+        s_c = torch.empty((B, H, D_COMPACT, D_V), dtype=torch.float32, device=s.device)
+    if z_c is None:
+        z_c = torch.empty((B, H, D_COMPACT), dtype=torch.float32, device=s.device)
+    _need(s_c, "s_c", (B, H, D_COMPACT, D_V), torch.float32)
+    _need(z_c, "z_c", (B, H, D_COMPACT), torch.float32)
+    _raise(lib.la_state_to_compact(_ptr(s), _ptr(z), _ptr(s_c), _ptr(z_c), B, H, D_FEAT, D_V,
+                                   _stream(stream)))
+    return s_c, z_c
+
+
+def state_from_compact(s_c, z_c, *, s=None, z=None, stream=None):
+    """la_state_from_compact: the compact layout -> the 273-row layout (cross
+    terms split evenly between (a, b) and (b, a))."""
+    lib = load_library()
+    B, H = s_c.shape[:2]
+    _need(s_c, "s_c", (B, H, D_COMPACT, D_V), torch.float32)
+    _need(z_c, "z_c", (B, H, D_COMPACT), torch.float32)
+    if s is None:
+        s = torch.empty((B, H, D_PHI, D_V), dtype=torch.float32, device=s_c.device)
+    if z is None:
+        z = torch.empty((B, H, D_PHI), dtype=torch.float32, device=s_c.device)
+    _need(s, "s", (B, H, D_PHI, D_V), torch.float32)
+    _need(z, "z", (B, H, D_PHI), torch.float32)
+    _raise(lib.la_state_from_compact(_ptr(s_c), _ptr(z_c), _ptr(s), _ptr(z), B, H, D_FEAT, D_V,
+                                     _stream(stream)))
+    return s, z
+
+
+def prefill_compact(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
+                    z_out=None, want_state: bool = True, stream=None):
+    """la_prefill_compact: causal prefill (bf16) with s0 [B,H,153,64], z0
+    [B,H,153] and the final state in the compact layout."""
+    lib = load_library()
+    B, H, N, _ = q.shape
+    dt = q.dtype
+    _need(q, "q", (B, H, N, D_FEAT), dt)
+    _need(k, "k", (B, H, N, D_FEAT), dt)
+    _need(v, "v", (B, H, N, D_V), dt)
+    if s0 is not None or z0 is not None:
+        _need(s0, "s0", (B, H, D_COMPACT, D_V), torch.float32)
+        _need(z0, "z0", (B, H, D_COMPACT), torch.float32)
+    if y is None:
+        y = torch.empty((B, H, N, D_V), dtype=dt, device=q.device)
+    _need(y, "y", (B, H, N, D_V), dt)
+    if want_state:
+        if s_out is None:
+            s_out = torch.empty((B, H, D_COMPACT, D_V), dtype=torch.float32, device=q.device)
+        if z_out is None:
+            z_out = torch.empty((B, H, D_COMPACT), dtype=torch.float32, device=q.device)
+    if s_out is not None:
+        _need(s_out, "s_out", (B, H, D_COMPACT, D_V), torch.float32)
+    if z_out is not None:
+        _need(z_out, "z_out", (B, H, D_COMPACT), torch.float32)
+    _raise(lib.la_prefill_compact(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y),
+                                  _ptr(s_out), _ptr(z_out), B, H, N, D_FEAT, D_V, _dt(q),
+                                  float(eps), _stream(stream)))
+    return y, s_out, z_out
+
+
+def decode_step_compact(q, k, v, s, z, *, eps: float = 0.0, y=None, s_out=None, z_out=None,
+                        inplace: bool = False, stream=None):
+    """la_decode_step_compact: one decode step on a compact state s
+    [B,H,153,64], z [B,H,153] fp32 (in place with inplace=True)."""
+    lib = load_library()
+    B, H, _ = q.shape
+    dt = q.dtype
+    _need(q, "q", (B, H, D_FEAT), dt)
+    _need(k, "k", (B, H, D_FEAT), dt)
+    _need(v, "v", (B, H, D_V), dt)
+    _need(s, "s", (B, H, D_COMPACT, D_V), torch.float32)
+    _need(z, "z", (B, H, D_COMPACT), torch.float32)
+    if inplace:
+        s_out, z_out = s, z
+    if s_out is None:
+        s_out = torch.empty_like(s)
+    if z_out is None:
+        z_out = torch.empty_like(z)
+    if y is None:
+        y = torch.empty((B, H, D_V), dtype=dt, device=q.device)
+    _raise(lib.la_decode_step_compact(_ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(z), _ptr(s_out),
+                                      _ptr(z_out), _ptr(y), B, H, D_FEAT, D_V, _dt(q), float(eps),
+                                      _stream(stream)))
     return y, s_out, z_out
 
 

@@ -103,7 +103,8 @@ cudaError_t run_prefill(const la::PrefillArgs &a, la_dtype dtype, cudaStream_t s
     const int64_t BH = a.B * a.H;
     if (a.N == 0) {
         if (!a.s_out && !a.z_out) return cudaSuccess;
-        return la::launch_state_copy(la::feat_dim(dk), a.s0, a.z0, a.s_out, a.z_out, BH, st);
+        return la::launch_state_copy(a.compact ? la::kDCompact : la::feat_dim(dk), a.s0, a.z0, a.s_out,
+                                     a.z_out, BH, st);
     }
     if (dk != kDFeat) return la::launch_prefill_general(a, dk, dtype, st);
     if (dtype == LA_DTYPE_BF16) return la::launch_prefill_tc(a, st);
@@ -143,12 +144,15 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 la_status prefill_impl(const void *q, const void *k, const void *v, const float *s0,
                        const float *z0, const int32_t *left_pad, void *y, float *s_out,
                        float *z_out, int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
-                       la_dtype dtype, float eps, la_stream_t stream, const float *gamma = nullptr) {
+                       la_dtype dtype, float eps, la_stream_t stream, const float *gamma = nullptr,
+                       bool compact = false) {
     la_status st = check_common(B, H, N, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
     // padding and decay exist for d' = 16 only
     if ((left_pad || gamma) && d_feat != kDFeat) return LA_ERR_UNSUPPORTED;
-    const int64_t D = la::feat_dim(d_feat);
+    // compact states: the bf16 tensor-core path of the plain prefill only
+    if (compact && (d_feat != kDFeat || dtype != LA_DTYPE_BF16 || left_pad || gamma)) return LA_ERR_UNSUPPORTED;
+    const int64_t D = compact ? la::kDCompact : la::feat_dim(d_feat);
     if ((s0 == nullptr) != (z0 == nullptr)) return LA_ERR_INVALID_ARG;
     if (N > 0 && (!q || !k || !v || !y)) return LA_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, s0, z0, y, s_out, z_out};
@@ -170,6 +174,7 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
     unsigned *status;
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
     la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad, gamma};
+    a.compact = compact;
     return to_status(run_prefill(a, dtype, reinterpret_cast<cudaStream_t>(stream), d_feat));
 }
 
@@ -288,11 +293,12 @@ namespace {
 la_status decode_impl(const void *q, const void *k, const void *v, const float *gamma,
                       const float *s_in, const float *z_in, float *s_out, float *z_out, void *y,
                       int64_t B, int64_t H, int d_feat, int d_v, la_dtype dtype, float eps,
-                      la_stream_t stream) {
+                      la_stream_t stream, bool compact = false) {
     la_status st = check_common(B, H, 1, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
     if (gamma && d_feat != kDFeat) return LA_ERR_UNSUPPORTED;  // decay exists for d' = 16 only
-    const int64_t D = la::feat_dim(d_feat);
+    if (compact && (d_feat != kDFeat || gamma)) return LA_ERR_UNSUPPORTED;
+    const int64_t D = compact ? la::kDCompact : la::feat_dim(d_feat);
     if (!q || !k || !v || !s_in || !z_in || !s_out || !z_out || !y) return LA_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, s_in, z_in, s_out, z_out, y};
     for (const void *p : ptrs)
@@ -318,6 +324,7 @@ la_status decode_impl(const void *q, const void *k, const void *v, const float *
     unsigned *status;
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
     la::DecodeArgs a{q, k, v, s_in, z_in, s_out, z_out, y, B, H, eps, gamma, status};
+    if (compact) return to_status(la::launch_decode_compact(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
     if (d_feat != kDFeat)
         return to_status(la::launch_decode_general(a, d_feat, dtype, reinterpret_cast<cudaStream_t>(stream)));
     return to_status(la::launch_decode(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
@@ -342,6 +349,65 @@ la_status la_decode_step_decay(const void *q, const void *k, const void *v, cons
     if (!gamma) return LA_ERR_INVALID_ARG;
     return decode_impl(q, k, v, gamma, s_in, z_in, s_out, z_out, y, B, H, d_feat, d_v, dtype, eps,
                        stream);
+}
+
+la_status la_decode_step_compact(const void *q, const void *k, const void *v, const float *s_in_c,
+                                 const float *z_in_c, float *s_out_c, float *z_out_c, void *y, int64_t B,
+                                 int64_t H, int d_feat, int d_v, la_dtype dtype, float eps,
+                                 la_stream_t stream) {
+    return decode_impl(q, k, v, nullptr, s_in_c, z_in_c, s_out_c, z_out_c, y, B, H, d_feat, d_v, dtype, eps,
+                       stream, true);
+}
+
+la_status la_prefill_compact(const void *q, const void *k, const void *v, const float *s0_c,
+                             const float *z0_c, void *y, float *s_out_c, float *z_out_c, int64_t B,
+                             int64_t H, int64_t N, int d_feat, int d_v, la_dtype dtype, float eps,
+                             la_stream_t stream) {
+    return prefill_impl(q, k, v, s0_c, z0_c, nullptr, y, s_out_c, z_out_c, B, H, N, d_feat, d_v, dtype, eps,
+                        stream, nullptr, true);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared checks of the two state conversions: from (rows_in) to (rows_out).
+la_status convert_check(const float *s_in, const float *z_in, const float *s_out, const float *z_out,
+                        int64_t B, int64_t H, int d_feat, int d_v, int64_t rows_in, int64_t rows_out,
+                        unsigned **status) {
+    if (d_feat != kDFeat || d_v != kDV) return LA_ERR_UNSUPPORTED;
+    if (B < 1 || H < 1 || B > kMaxBH / H) return LA_ERR_INVALID_ARG;
+    if (!s_in || !z_in || !s_out || !z_out) return LA_ERR_INVALID_ARG;
+    const void *ptrs[] = {s_in, z_in, s_out, z_out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return LA_ERR_MISALIGNED;
+    const int64_t BH = B * H;
+    const Range in[] = {{s_in, sizeof(float) * BH * rows_in * kDV}, {z_in, sizeof(float) * BH * rows_in}};
+    const Range out[] = {{s_out, sizeof(float) * BH * rows_out * kDV}, {z_out, sizeof(float) * BH * rows_out}};
+    if (any_overlap(in, 2, out, 2)) return LA_ERR_INVALID_ARG;
+    int dev;
+    return device_setup(&dev, status);
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status la_state_to_compact(const float *s, const float *z, float *s_c, float *z_c, int64_t B, int64_t H,
+                              int d_feat, int d_v, la_stream_t stream) {
+    unsigned *status;
+    la_status st = convert_check(s, z, s_c, z_c, B, H, d_feat, d_v, kD, la::kDCompact, &status);
+    if (st != LA_OK) return st;
+    return to_status(la::launch_state_to_compact(s, z, s_c, z_c, B * H, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+la_status la_state_from_compact(const float *s_c, const float *z_c, float *s, float *z, int64_t B, int64_t H,
+                                int d_feat, int d_v, la_stream_t stream) {
+    unsigned *status;
+    la_status st = convert_check(s_c, z_c, s, z, B, H, d_feat, d_v, la::kDCompact, kD, &status);
+    if (st != LA_OK) return st;
+    return to_status(
+        la::launch_state_from_compact(s_c, z_c, s, z, B * H, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 la_status la_prefill_decay(const void *q, const void *k, const void *v, const float *s0,

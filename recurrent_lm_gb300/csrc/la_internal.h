@@ -43,6 +43,7 @@ struct PrefillArgs {
     unsigned *status;   // device status word
     const int32_t *left_pad;  // [B] leading padding positions per batch row, or NULL
     const float *gamma;       // [H] per-head decay in [0, 1], or NULL (no decay)
+    bool compact = false;     // s0/z0 and s_out/z_out in the 153-row compact layout
 };
 
 struct DecodeArgs {
@@ -90,5 +91,13 @@ cudaError_t launch_prefix_reduce(const PrefixArgs &a, cudaStream_t st);
 cudaError_t launch_state_copy(int64_t D, const float *s0, const float *z0, float *s_out,
                               float *z_out, int64_t BH, cudaStream_t st);
 cudaError_t launch_timeout_probe(unsigned *status, cudaStream_t st);
+
+// Compact state layout (d' = 16): 153 rows, see linattn.h.
+constexpr int kDCompact = 153;
+cudaError_t launch_decode_compact(const DecodeArgs &a, la_dtype dt, cudaStream_t st);
+cudaError_t launch_state_to_compact(const float *s, const float *z, float *s_c, float *z_c, int64_t BH,
+                                    cudaStream_t st);
+cudaError_t launch_state_from_compact(const float *s_c, const float *z_c, float *s, float *z, int64_t BH,
+                                      cudaStream_t st);
 
 }  // namespace la

@@ -232,6 +232,7 @@ static __device__ __noinline__ bool p_block(uint32_t tsrc, uint32_t tdst, int pp
 // feature-operand buffers it overlays are free by then).
 constexpr uint32_t kSmStage = kSmPhiQ;
 constexpr uint32_t kStageBytes = (uint32_t)kD * kDV * 4;
+constexpr uint32_t kStageBytesCompact = (uint32_t)kDCompact * kDV * 4;  // the 153-row layout
 static_assert(kSmStage + kStageBytes <= kSmSb, "final state image overlays Phi'_Q and Phi'_K only");
 
 // Optional per-role timeline of CTA 0 (compile with -DLA_TRACE): SM clock
@@ -256,7 +257,7 @@ enum { TR_TMA = 0, TR_MMA, TR_GEN, TR_EPI, TR_CONV };
 // writes gamma^(L-1-t) Phi'_K (scaled key features), the intra-chunk kernel
 // entries carry gamma^(i-j), and the state is multiplied by gamma^L in TMEM
 // before each update.
-template <bool kPad, bool kDecay>
+template <bool kPad, bool kDecay, bool kCompact = false>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty,
@@ -280,11 +281,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int n = (N + kC - 1) / kC;
     // leading padding positions of this batch row: no contribution to any sum, y = 0
     const int lpad = kPad ? (int)row_left_pad(left_pad, bh / H, N, status, tid == 0) : 0;
-    // per-head columns of the ABI state: entry (row r, value d) at [r * 64 + d]
-    const float *s0h = s0 ? s0 + bh * (int64_t)kD * kDV : nullptr;
-    const float *z0h = z0 ? z0 + bh * (int64_t)kD : nullptr;
-    float *s_outh = s_out ? s_out + bh * (int64_t)kD * kDV : nullptr;
-    float *z_outh = z_out ? z_out + bh * (int64_t)kD : nullptr;
+    // per-head columns of the state in memory (the 273-row layout, or with
+    // kCompact the 153-row one): entry (row r, value d) at [r * 64 + d]
+    constexpr int64_t kRowsIO = kCompact ? kDCompact : kD;
+    const float *s0h = s0 ? s0 + bh * kRowsIO * kDV : nullptr;
+    const float *z0h = z0 ? z0 + bh * kRowsIO : nullptr;
+    float *s_outh = s_out ? s_out + bh * kRowsIO * kDV : nullptr;
+    float *z_outh = z_out ? z_out + bh * kRowsIO : nullptr;
 
     // ---- set-up: barriers, TMEM, constant operands, feature -> row table
     if (tid == 0) {
@@ -374,7 +377,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         auto load_group = [&](auto gc) {
             constexpr int G = decltype(gc)::value;
             uint32_t r[32];
-            compact_initial_group<G>(col0, stride, r, std::make_integer_sequence<int, 32>{});
+            if constexpr (kCompact)
+                compact_io_initial_group<G>(col0, stride, r, std::make_integer_sequence<int, 32>{});
+            else
+                compact_initial_group<G>(col0, stride, r, std::make_integer_sequence<int, 32>{});
             __syncwarp();
             if (!zrow || lane == 0) write_sb_group(sb + kSmSb, zrow ? 64 : d, G, r);
             if constexpr (kDecay) {  // the first update starts from gamma^L0 s0
@@ -422,7 +428,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 mbar_expect_tx(bar(B_V_FULL + st), kC * 64 * 2);
                 tma_load_3d(sb + kSmV + st * 16384, &tv, bar(B_V_FULL + st), 0, c * kC, (int)bh);
                 issued_v = c + 1;
-                if (c == n - 1 && s0h) {
+                if (!kCompact && c == n - 1 && s0h) {
                     // the final state store reads s0 again (its antisymmetric part)
                     prefetch_l2_bulk(s0h, (uint32_t)kD * kDV * 4);
                     for (int o = 0; o < kD; o += 32) prefetch_l2(z0h + o);
@@ -607,15 +613,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             __syncwarp();
             tc_fence_after();
             if (tid == 128) LA_TR(TR_CONV, n - 1, 4);
-            if (wq < 3)
-                final_groups<true, 3>(tmem + lanebase + kTmS, 32 * wq + lane, zrow, lane, s0h, sb + kSmStage,
-                                      s_outh, z0h, z_outh, anti_decay, std::make_integer_sequence<int, 2>{});
+            if (wq < 3) {
+                if constexpr (kCompact)
+                    final_groups_compact<true, 3>(tmem + lanebase + kTmS, 32 * wq + lane, zrow, lane,
+                                                  sb + kSmStage, s_outh, z_outh, std::make_integer_sequence<int, 2>{});
+                else
+                    final_groups<true, 3>(tmem + lanebase + kTmS, 32 * wq + lane, zrow, lane, s0h, sb + kSmStage,
+                                          s_outh, z0h, z_outh, anti_decay, std::make_integer_sequence<int, 2>{});
+            }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_STAGED));
             // every value row is in the image: one bulk copy to s_out
             if (tid == 128 && s_outh && mbar_wait(bar(B_STAGED), 0u, abort, status)) {
-                bulk_store(s_outh, sb + kSmStage, kStageBytes);
+                bulk_store(s_outh, sb + kSmStage, kCompact ? kStageBytesCompact : kStageBytes);
                 bulk_commit();
                 bulk_wait0();
             }
@@ -670,6 +681,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     convert_groups<0, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                     __syncwarp();
                     convert_groups<2, 1, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
+                } else if constexpr (kCompact) {
+                    final_groups_compact<true, 0>(tmem + lanebase + kTmS, i, zrow, lane, sb + kSmStage, s_outh,
+                                                  z_outh, std::make_integer_sequence<int, 3>{});
                 } else {
                     final_groups<true, 0>(tmem + lanebase + kTmS, i, zrow, lane, s0h, sb + kSmStage, s_outh, z0h,
                                           z_outh, anti_decay, std::make_integer_sequence<int, 3>{});
@@ -824,11 +838,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(prefill_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kSmAlloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<false, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
     if (a.left_pad && a.gamma) return cudaErrorInvalidValue;  // no padded decayed variant
-    if (a.left_pad)
+    if (a.compact && (a.left_pad || a.gamma)) return cudaErrorInvalidValue;  // plain prefill only
+    if (a.compact)
+        prefill_tc_kernel<false, false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
+            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+    else if (a.left_pad)
         prefill_tc_kernel<true, false><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
             tq, tk, tv, ty, a.s0, a.z0, a.left_pad, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
     else if (a.gamma)

@@ -324,5 +324,92 @@ static __device__ __noinline__ void final_groups(uint32_t taddr, int d, bool zro
     (final_group_rows<kStage, G0 + I>(taddr, d, zrow, lane, s0h, stage, s_outh, z0h, z_outh, anti_scale), ...);
 }
 
+// ---- compact state layout in memory (153 rows: 0 constant, 1 + a linear,
+// 17 + c(a, b) quadratic for a <= b, c(a, b) = 16 a - a (a - 1) / 2 + (b - a)),
+// with the symmetric map of the BASED notes, sec. 2.3: squares carry 1/sqrt2
+// on both sides, cross terms none.  The internal entry of a square is then
+// the memory entry / sqrt2 (the internal key side carries xbar_a^2 / 2), every
+// other internal entry equals its memory entry.  kDCompact (153) is la::kDCompact.
+
+// Row of compact feature f in the 153-row layout, -1 for padding.
+__host__ __device__ constexpr int compact_row(int f) {
+    const Rows e = abi_rows(f);
+    if (e.kind == 3) return -1;
+    if (e.kind == 2) return e.r1;  // constant and linear rows coincide with the 273-row layout
+    const int x = (e.r1 - 17) / 16, y = (e.r1 - 17) % 16;
+    const int a = x < y ? x : y, b = x < y ? y : x;
+    return 17 + 16 * a - a * (a - 1) / 2 + (b - a);
+}
+static_assert(compact_row(0) == 17 && compact_row(152) == 0 && compact_row(153) == -1, "compact rows");
+
+template <int F>
+__device__ __forceinline__ float compact_io_read(const float *col, int64_t stride) {
+    constexpr int r = compact_row(F);
+    if constexpr (r < 0) return 0.f;
+    else return __ldcg(col + r * stride);
+}
+
+template <int F>
+__device__ __forceinline__ uint32_t compact_io_entry(float x) {
+    constexpr Rows e = abi_rows(F);
+    if constexpr (e.kind == 3) return 0u;
+    else if constexpr (e.kind == 0) return __float_as_uint(x * kRSqrt2);
+    else return __float_as_uint(x);
+}
+
+// Internal entries of the initial state for the 32 features of group G from
+// the compact-layout column `col` (NULL: zero state); every read is issued
+// before any is used.
+template <int G, int... J>
+__device__ __forceinline__ void compact_io_initial_group(const float *col, int64_t stride, uint32_t (&r)[32],
+                                                         std::integer_sequence<int, J...>) {
+    if (!col) {
+        ((r[J] = 0u), ...);
+        return;
+    }
+    float a[32];
+    ((a[J] = compact_io_read<32 * G + J>(col, stride)), ...);
+    ((r[J] = compact_io_entry<32 * G + J>(a[J])), ...);
+}
+
+// Memory entry of compact feature F from its internal entry x: written into
+// the shared-memory image at stage_d + 256 * row (kStage) or to out[row * stride].
+template <bool kStage, int F>
+__device__ __forceinline__ void compact_io_write(float x, uint32_t stage_d, float *out, int64_t stride) {
+    constexpr Rows e = abi_rows(F);
+    constexpr int r = compact_row(F);
+    if constexpr (r < 0) return;
+    else {
+        const float v = e.kind == 0 ? x * kSqrt2 : x;
+        if constexpr (kStage) st_shared_f32(stage_d + 256u * (uint32_t)r, v);
+        else out[r * stride] = v;
+    }
+}
+
+// Final compact-layout state of feature group G from TMEM rows (the
+// counterpart of final_group_rows; there is no antisymmetric part to add).
+template <bool kStage, int G, int... J>
+__device__ __forceinline__ void final_group_rows_compact(uint32_t taddr, int d, bool zrow, int lane,
+                                                         uint32_t stage, float *s_outh, float *z_outh,
+                                                         std::integer_sequence<int, J...>) {
+    uint32_t r[32];
+    tmem_load32_sync(taddr + 32 * G, r);
+    if (zrow) {
+        if (lane == 0 && z_outh) (compact_io_write<false, 32 * G + J>(__uint_as_float(r[J]), 0u, z_outh, 1), ...);
+    } else if (kStage || s_outh) {
+        (compact_io_write<kStage, 32 * G + J>(__uint_as_float(r[J]), stage + 4u * (uint32_t)d,
+                                              s_outh ? s_outh + d : nullptr, kDV), ...);
+    }
+    __syncwarp();
+}
+
+template <bool kStage, int G0, int... I>
+static __device__ __noinline__ void final_groups_compact(uint32_t taddr, int d, bool zrow, int lane,
+                                                         uint32_t stage, float *s_outh, float *z_outh,
+                                                         std::integer_sequence<int, I...>) {
+    (final_group_rows_compact<kStage, G0 + I>(taddr, d, zrow, lane, stage, s_outh, z_outh,
+                                              std::make_integer_sequence<int, 32>{}), ...);
+}
+
 }  // namespace taylor
 }  // namespace la

@@ -230,3 +230,44 @@ def test_host_prefill_rejects_bad_args(lib):
     # buffers are accepted, so they could)
     assert call_host(lib, p, ctypes.c_void_p(p[0].value + 256), need) == binding.LA_ERR_INVALID_ARG
     assert call_host(lib, p, ctypes.c_void_p(p[6].value), need) == binding.LA_ERR_INVALID_ARG
+
+
+def test_compact_calls_reject_bad_args(lib):
+    """The compact-state calls: d' = 16 and d_v = 64 only, bf16 only for the
+    prefill, required pointers, 16-byte alignment, no overlap (the overlap
+    ranges use the 153-row sizes)."""
+    p = [fake(i) for i in range(8)]
+    # decode: dims, shapes, NULL, alignment, partial overlap of the compact state
+    assert lib.la_decode_step_compact(*p, 4, 2, 8, 64, 1, 0.0, None) == binding.LA_ERR_UNSUPPORTED
+    assert lib.la_decode_step_compact(*p, 4, 2, 16, 32, 1, 0.0, None) == binding.LA_ERR_UNSUPPORTED
+    assert lib.la_decode_step_compact(*p, 0, 2, 16, 64, 1, 0.0, None) == binding.LA_ERR_INVALID_ARG
+    q = list(p); q[4] = None
+    assert lib.la_decode_step_compact(*q, 4, 2, 16, 64, 1, 0.0, None) == binding.LA_ERR_INVALID_ARG
+    q = list(p); q[6] = fake(6, misalign=4)
+    assert lib.la_decode_step_compact(*q, 4, 2, 16, 64, 1, 0.0, None) == binding.LA_ERR_MISALIGNED
+    # s_out starts inside s_in's last head: 153 rows * 64 * 4 B per head, 8 heads
+    q = list(p); q[5] = ctypes.c_void_p(p[3].value + 8 * 153 * 256 - 256)
+    assert lib.la_decode_step_compact(*q, 4, 2, 16, 64, 1, 0.0, None) == binding.LA_ERR_INVALID_ARG
+    q = list(p); q[5] = ctypes.c_void_p(p[3].value + 8 * 153 * 256)   # just past it: fine up to the device
+    assert lib.la_decode_step_compact(*q, 4, 2, 16, 64, 1, 0.0, None) not in (
+        binding.LA_ERR_INVALID_ARG, binding.LA_ERR_MISALIGNED, binding.LA_ERR_UNSUPPORTED)
+    # prefill: fp32 activations and d' != 16 are unsupported; half state is invalid
+    assert lib.la_prefill_compact(*p, 1, 1, 8, 16, 64, 0, 0.0, None) == binding.LA_ERR_UNSUPPORTED
+    assert lib.la_prefill_compact(*p, 1, 1, 8, 8, 64, 1, 0.0, None) == binding.LA_ERR_UNSUPPORTED
+    q = list(p); q[4] = None
+    assert lib.la_prefill_compact(*q, 1, 1, 8, 16, 64, 1, 0.0, None) == binding.LA_ERR_INVALID_ARG
+    q = list(p); q[6] = ctypes.c_void_p(p[3].value)
+    assert lib.la_prefill_compact(*q, 1, 1, 8, 16, 64, 1, 0.0, None) == binding.LA_ERR_INVALID_ARG
+    # conversions
+    c = [fake(i) for i in range(4)]
+    for fn in (lib.la_state_to_compact, lib.la_state_from_compact):
+        assert fn(*c, 2, 3, 16, 48, None) == binding.LA_ERR_UNSUPPORTED
+        assert fn(*c, 2, 3, 24, 64, None) == binding.LA_ERR_UNSUPPORTED
+        assert fn(*c, 0, 3, 16, 64, None) == binding.LA_ERR_INVALID_ARG
+        for i in range(4):
+            d = list(c); d[i] = None
+            assert fn(*d, 2, 3, 16, 64, None) == binding.LA_ERR_INVALID_ARG
+            d = list(c); d[i] = fake(i, misalign=8)
+            assert fn(*d, 2, 3, 16, 64, None) == binding.LA_ERR_MISALIGNED
+        d = list(c); d[2] = ctypes.c_void_p(c[0].value + 1024)
+        assert fn(*d, 2, 3, 16, 64, None) == binding.LA_ERR_INVALID_ARG

@@ -106,16 +106,20 @@ def test_decode_full_batch_sampled_heads():
 def test_decode_graph_pipeline_full_batch():
     """The benchmark's decode pipeline: B=128, H=16, the state from a 2048-token
     GPU prefill, then T=128 consecutive in-place decode steps captured in one
-    CUDA graph and replayed.  Every step's y and the final state of 8 sampled
-    heads against the oracle run from the same initial state."""
+    CUDA graph and replayed.  The oracle runs its own prefill of the 8 sampled
+    heads' 2048 tokens (checked against the GPU's), then every step's y and
+    the final state of those heads are checked against the oracle's steps."""
     w = inputs.WORKLOADS[5]
     B, H, T = w.B, w.H, 128
     qs, ks, vs = inputs.s0_sequence(5)
     _, s, z = la.prefill(qs.to(DEV), ks.to(DEV), vs.to(DEV))
     torch.cuda.synchronize()
     heads = sample_heads(B, H, 8, seed=6)
-    s_r = torch.stack([s[b, h] for b, h in heads])[None].double().cpu().numpy()
-    z_r = torch.stack([z[b, h] for b, h in heads])[None].double().cpu().numpy()
+    pick = lambda t: torch.stack([t[b, h] for b, h in heads])[None]
+    _, s_r, z_r = oracle.prefill(pick(qs), pick(ks), pick(vs))
+    tol = TOL[torch.bfloat16]
+    assert_close("prefill s", pick(s), s_r, tol)
+    assert_close("prefill z", pick(z), z_r, tol)
     steps = [inputs.decode_step_inputs(5, i) for i in range(T)]
     qd = torch.stack([t[0] for t in steps]).to(DEV)
     kd = torch.stack([t[1] for t in steps]).to(DEV)
@@ -134,7 +138,6 @@ def test_decode_graph_pipeline_full_batch():
     graph.replay()
     torch.cuda.synchronize()
     la.check_device_status()
-    tol = TOL[torch.bfloat16]
     for i, (q, k, v) in enumerate(steps):
         qq, kk, vv = (torch.stack([t[b, h] for b, h in heads])[None] for t in (q, k, v))
         y_r, s_r, z_r = oracle.decode_step(qq, kk, vv, s_r, z_r)
