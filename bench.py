@@ -56,6 +56,7 @@ BYTES_PER_HEAD_TOKEN_BF16 = 320     # q 32 + k 32 + v 128 + y 128
 BYTES_PER_PREFIX_TOKEN_BF16 = 160   # k_e 32 + v_e 128
 STATE_BYTES = 273 * 64 * 4 + 273 * 4  # one head's s and z (fp32)
 COMPACT_STATE_BYTES = 153 * 64 * 4 + 153 * 4  # the same in the 153-row compact layout
+COMPACT_LAYERS = 3   # compact decode leg: 3 x 81.5 MB of state, about 1.9x L2
 
 
 def log(*a):
@@ -425,16 +426,24 @@ def leg_general_dk(la, args, dist, dev):
 def leg_decode(la, args, dist, dev, decay: bool = False, compact: bool = False):
     """512 decode steps in one CUDA graph (with decay: la_decode_step_decay;
     compact: the 153-row state from la_prefill_compact and
-    la_decode_step_compact)."""
+    la_decode_step_compact).  The 273-row state (143 MB at B=128, H=16) is
+    larger than L2; the compact one (81.5 MB) is not, so that leg keeps
+    COMPACT_LAYERS independent states (as the layers of a model would) and
+    runs each step over all of them in turn: every state leaves L2 before it
+    is used again, and the time per layer-step is reported."""
     w = inputs.WORKLOADS[5]
     B, H, T = w.B, w.H, args.decode_steps
+    layers = COMPACT_LAYERS if compact else 1
     g = torch.Generator(device=dev)
     g.manual_seed(shard_seed(w.seed, dist.rank))
-    qs = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
-    ks = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
-    vs = gen_device((B, H, w.s0_tokens, 64), g, dev=dev)
-    _, s, z = (la.prefill_compact if compact else la.prefill)(qs, ks, vs)
-    del qs, ks, vs
+    states = []
+    for _ in range(layers):
+        qs = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
+        ks = gen_device((B, H, w.s0_tokens, 16), g, dev=dev)
+        vs = gen_device((B, H, w.s0_tokens, 64), g, dev=dev)
+        _, s, z = (la.prefill_compact if compact else la.prefill)(qs, ks, vs)
+        states.append((s, z))
+        del qs, ks, vs
     qd = gen_device((T, B, H, 16), g, dev=dev)
     kd = gen_device((T, B, H, 16), g, dev=dev)
     vd = gen_device((T, B, H, 64), g, dev=dev)
@@ -442,10 +451,11 @@ def leg_decode(la, args, dist, dev, decay: bool = False, compact: bool = False):
     gam = decay_rates(H, dev) if decay else None
 
     def one(i):
-        if compact:
-            la.decode_step_compact(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True)
-        else:
-            la.decode_step(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True, gamma=gam)
+        for s, z in states:
+            if compact:
+                la.decode_step_compact(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True)
+            else:
+                la.decode_step(qd[i], kd[i], vd[i], s, z, y=yd[i], inplace=True, gamma=gam)
     # warm up the library (per-device set-up) before capture
     one(0)
     torch.cuda.synchronize()
@@ -460,7 +470,8 @@ def leg_decode(la, args, dist, dev, decay: bool = False, compact: bool = False):
     ms = time_loop(graph.replay, max(1, args.steps // 4), max(3, args.warmup // 2), dist)
     la.check_device_status()
     ok = bool(torch.isfinite(yd[-1].float()).all().item() and torch.isfinite(s[0, 0]).all().item())
-    return {"ms_per_graph": ms, "steps_per_graph": T, "B": B, "H": H, "finite": ok}
+    return {"ms_per_graph": ms, "steps_per_graph": T * layers, "layers": layers, "B": B, "H": H,
+            "finite": ok}
 
 
 def cpu_baseline_prefill(sample_rows: int):
@@ -486,7 +497,8 @@ def ncu_case(la, case: str):
     initial state, two launches each (DRAM traffic is linear in N, so the
     full-length launch is extrapolated from the two sizes); decode (273-row or
     compact state) at the bench batch B=128, H=16, ten steps in place back to
-    back (inputs generated first, so that nothing runs between the steps);
+    back (inputs generated first, so that nothing runs between the steps; the
+    compact case over the bench leg's independent states in turn);
     prefix N=M=4096, three calls."""
     dev = "cuda:0"
     g = torch.Generator(device=dev)
@@ -505,17 +517,20 @@ def ncu_case(la, case: str):
             del q, k, v
     elif case in ("decode", "decode_compact"):
         B, H, T = 128, 16, 10
-        D = 153 if case == "decode_compact" else 273
-        s = torch.randn(B, H, D, 64, device=dev, generator=g)
-        z = torch.rand(B, H, D, device=dev, generator=g) + 100.0
+        compact = case == "decode_compact"
+        D = 153 if compact else 273
+        layers = COMPACT_LAYERS if compact else 1   # as in the bench leg
+        states = [(torch.randn(B, H, D, 64, device=dev, generator=g),
+                   torch.rand(B, H, D, device=dev, generator=g) + 100.0) for _ in range(layers)]
         q = gen_device((T, B, H, 16), g, dev=dev)
         k = gen_device((T, B, H, 16), g, dev=dev)
         v = gen_device((T, B, H, 64), g, dev=dev)
         y = torch.empty((T, B, H, 64), dtype=torch.bfloat16, device=dev)
-        step = la.decode_step_compact if case == "decode_compact" else la.decode_step
+        step = la.decode_step_compact if compact else la.decode_step
         torch.cuda.synchronize()
         for i in range(T):
-            step(q[i], k[i], v[i], s, z, y=y[i], inplace=True)
+            for s, z in states:
+                step(q[i], k[i], v[i], s, z, y=y[i], inplace=True)
     elif case == "prefix":
         B, H, N, M = 16, 16, 4096, 4096
         q, k = gen_device((B, H, N, 16), g, dev=dev), gen_device((B, H, N, 16), g, dev=dev)
@@ -699,6 +714,11 @@ def main():
                          "traffic": kernel_traffic(dname) if dname != "decode_decay" else None,
                          "algorithmic_bytes_per_launch": by},
             "cuda_graph_steps": r["steps_per_graph"], "finite": r["finite"]}
+        if r["layers"] > 1:
+            line["legs"][dname]["layers"] = r["layers"]
+            line["legs"][dname]["l2"] = (f"{r['layers']} independent B={r['B']} H={r['H']} states, "
+                                         f"{r['layers'] * bh * sbytes / 1e6:.0f} MB, visited in turn "
+                                         "each step (larger than L2); us_per_step is per layer-step")
         launches += r["steps_per_graph"] * max(1, args.steps // 4)
     line["gpu_launches"] = launches
     line["gpu_launches_note"] = ("prefill leg: 1 kernel per step; prefix leg: 3 per call; "

@@ -364,8 +364,10 @@ LA_API la_status la_decode_step_compact(const void *q, const void *k, const void
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before capturing the stream into a CUDA graph.
  *   - Problems with la_prefix_workspace_size(B, H, M) larger than the buffer
- *     return LA_ERR_SCRATCH_TOO_SMALL before any work is queued; roughly
- *     B*H*(ceil(M/2048) + 1) <= 472 fits.
+ *     return LA_ERR_SCRATCH_TOO_SMALL before any work is queued.  The
+ *     workspace holds B*H*nseg partial states of 70,980 bytes, with nseg =
+ *     min(16, ceil(256 / (B*H)), ceil(M / 128)) prefix segments (fewer once
+ *     their length is rounded up to 128 tokens), so B*H*nseg <= 472 fits.
  *   - Every call on a device shares the buffer, and the buffer keeps the last
  *     call's contents.  Nothing in it needs to start at zero (each call
  *     writes every part it reads).  Calls whose work overlaps on the GPU (two

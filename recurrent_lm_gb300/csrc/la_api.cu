@@ -82,19 +82,20 @@ size_t esize(la_dtype dt) { return dt == LA_DTYPE_BF16 ? 2 : 4; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace of the prefix call: the per-segment partial states, sized for
+// the 273-row layout of the fp32 path (the bf16 path uses the first 160 rows'
+// worth of each part).
 struct PrefixLayout {
-    size_t part_s, part_z, s_init, z_init, total;
+    size_t part_s, part_z, total;
 };
 
 PrefixLayout prefix_layout(int64_t BH, int64_t M) {
     PrefixLayout L{};
     if (M <= 0) return L;
-    const int64_t nseg = la::prefix_nseg(M);
+    const int64_t nseg = la::prefix_split(BH, M).nseg;
     size_t off = 0;
     L.part_s = off; off = align256(off + sizeof(float) * BH * nseg * kD * kDV);
     L.part_z = off; off = align256(off + sizeof(float) * BH * nseg * kD);
-    L.s_init = off; off = align256(off + sizeof(float) * BH * kD * kDV);
-    L.z_init = off; off = align256(off + sizeof(float) * BH * kD);
     L.total = off;
     return L;
 }
@@ -219,23 +220,25 @@ la_status prefix_impl(const void *q, const void *k, const void *v, const void *k
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
 
     char *ws = static_cast<char *>(workspace);
+    const la::PrefixSplit split = la::prefix_split(BH, M);
     la::PrefixArgs pa{};
     pa.k_e = k_e; pa.v_e = v_e; pa.B = B; pa.H = H; pa.M = M;
-    pa.seg_len = la::kPrefixSeg; pa.nseg = la::prefix_nseg(M);
+    pa.seg_len = split.seg_len; pa.nseg = split.nseg;
     pa.part_s = reinterpret_cast<float *>(ws + L.part_s);
     pa.part_z = reinterpret_cast<float *>(ws + L.part_z);
-    pa.s0 = s0; pa.z0 = z0;
-    pa.s_init = reinterpret_cast<float *>(ws + L.s_init);
-    pa.z_init = reinterpret_cast<float *>(ws + L.z_init);
     pa.status = status;
     pa.left_pad = left_pad;
     pa.N = N;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // the partial states, then the prefill, whose set-up adds them (in segment
+    // order) to s0, z0
     cudaError_t e = dtype == LA_DTYPE_BF16 ? la::launch_prefix_partials_tc(pa, cs)
                                            : la::launch_prefix_partials_simt(pa, dtype, cs);
-    if (e == cudaSuccess) e = la::launch_prefix_reduce(pa, cs);
     if (e != cudaSuccess) return LA_ERR_CUDA;
-    la::PrefillArgs a{q, k, v, pa.s_init, pa.z_init, y, s_out, z_out, B, H, N, eps, status, left_pad};
+    la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad};
+    a.part_s = pa.part_s;
+    a.part_z = pa.part_z;
+    a.nseg = pa.nseg;
     return to_status(run_prefill(a, dtype, cs));
 }
 

@@ -44,6 +44,12 @@ struct PrefillArgs {
     const int32_t *left_pad;  // [B] leading padding positions per batch row, or NULL
     const float *gamma;       // [H] per-head decay in [0, 1], or NULL (no decay)
     bool compact = false;     // s0/z0 and s_out/z_out in the 153-row compact layout
+    // Prefix partial states added, segment by segment in order, to the initial
+    // state (NULL: none): the bf16 tensor-core path reads its internal compact
+    // rows, part_s [BH][nseg][160][64] and part_z [BH][nseg][160]; the fp32
+    // path the 273-row ones, part_s [BH][nseg][273][64] and part_z [BH][nseg][273].
+    const float *part_s = nullptr, *part_z = nullptr;
+    int64_t nseg = 0;
 };
 
 struct DecodeArgs {
@@ -57,23 +63,34 @@ struct DecodeArgs {
     unsigned *status;
 };
 
-// Per-segment partial prefix states: part_s [BH][nseg][273][64],
-// part_z [BH][nseg][273] (fp32), reduced into s0' / z0'.
+// Per-segment partial prefix states (fp32), in the layouts PrefillArgs
+// describes; the prefill adds them to its initial state.
 struct PrefixArgs {
     const void *k_e, *v_e;
     int64_t B, H, M;
     int64_t seg_len, nseg;
     float *part_s, *part_z;
-    const float *s0, *z0;
-    float *s_init, *z_init;   // s0 + s_E, z0 + z_E  [BH][273][64], [BH][273]
     unsigned *status;
     const int32_t *left_pad;  // [B]: prefix positions j < min(left_pad[b], M) are padding
     int64_t N;                // causal length (the range of left_pad)
 };
 
-// Token-segment length of the prefix reduction and its workspace layout.
-constexpr int64_t kPrefixSeg = 2048;
-inline int64_t prefix_nseg(int64_t M) { return (M + kPrefixSeg - 1) / kPrefixSeg; }
+// Split of the M prefix tokens into segments, one CTA each: enough segments
+// for about 256 CTAs over all (b, h) (at most 16 per head, at least one
+// 128-token chunk each), segment length a multiple of 128.
+struct PrefixSplit {
+    int64_t seg_len, nseg;
+};
+inline PrefixSplit prefix_split(int64_t BH, int64_t M) {
+    if (M <= 0 || BH <= 0) return {0, 0};
+    int64_t n = (256 + BH - 1) / BH;
+    if (n > 16) n = 16;
+    const int64_t chunks = (M + 127) / 128;
+    if (n > chunks) n = chunks;
+    const int64_t seg_len = (M + n - 1) / n;
+    const int64_t seg = (seg_len + 127) / 128 * 128;
+    return {seg, (M + seg - 1) / seg};
+}
 
 // Feature dimensions d' with a kernel: 16 (tensor-core and CUDA-core paths)
 // and 8, 24, 32 (the general CUDA-core path).  D = 1 + d' + d'^2.
@@ -87,7 +104,6 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, la_dtype dt, cudaStream_t 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st);
 cudaError_t launch_prefix_partials_simt(const PrefixArgs &a, la_dtype dt, cudaStream_t st);
 cudaError_t launch_prefix_partials_tc(const PrefixArgs &a, cudaStream_t st);
-cudaError_t launch_prefix_reduce(const PrefixArgs &a, cudaStream_t st);
 cudaError_t launch_state_copy(int64_t D, const float *s0, const float *z0, float *s_out,
                               float *z_out, int64_t BH, cudaStream_t st);
 cudaError_t launch_timeout_probe(unsigned *status, cudaStream_t st);

@@ -1,7 +1,8 @@
 // CUDA-core (fp32 FFMA) kernels: the token-by-token prefill used for fp32
-// activations, the per-segment prefix-state partial sums for fp32
-// activations, the deterministic reduction of prefix partials into the
-// initial state, and the state copy used when N == 0.
+// activations (its initial state is s0 plus, for the prefix call, the
+// per-segment prefix partial states added in segment order, so the sum is
+// deterministic), the per-segment prefix-state partial sums for fp32
+// activations, and the state copy used when N == 0.
 //
 // Prefill: BASED reading notes ("Simple linear attention language models
 // balance the recall-throughput tradeoff"), sec. 2.2 Eqs. (1)-(3); initial
@@ -42,7 +43,8 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
                     const float *__restrict__ z0, T *__restrict__ y,
                     float *__restrict__ s_out, float *__restrict__ z_out,
                     int64_t N, float eps, const int32_t *__restrict__ left_pad, int64_t H,
-                    unsigned *status, const float *__restrict__ gamma) {
+                    unsigned *status, const float *__restrict__ gamma,
+                    const float *__restrict__ part_s, const float *__restrict__ part_z, int64_t nseg) {
     __shared__ float xq[kDFeat], xk[kDFeat], vs[kDV];
     __shared__ float phq[kD], phk[kD];
     __shared__ float zsh[kD];
@@ -60,6 +62,17 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k,
         s[j] = (s0 && r < kD) ? s0[(bh * kD + r) * kDV + c] : 0.f;
     }
     for (int f = tid; f < kD; f += kThreads) zsh[f] = z0 ? z0[bh * kD + f] : 0.f;
+    // prefix call: + the partial states of the prefix segments, in order
+    for (int64_t sg = 0; part_s && sg < nseg; ++sg) {
+        const float *ps = part_s + (bh * nseg + sg) * (int64_t)kD * kDV;
+#pragma unroll
+        for (int j = 0; j < kRowsPerThread; ++j) {
+            const int r = g + j * kRowGroups;
+            if (r < kD) s[j] += ps[r * kDV + c];
+        }
+        const float *pz = part_z + (bh * nseg + sg) * (int64_t)kD;
+        for (int f = tid; f < kD; f += kThreads) zsh[f] += pz[f];
+    }
 
     // leading padding positions of this batch row: y = 0, no state change
     const int64_t lpad = row_left_pad(left_pad, bh / H, N, status, tid == 0);
@@ -181,33 +194,6 @@ prefix_partial_simt_kernel(const T *__restrict__ ke, const T *__restrict__ ve,
     for (int f = tid; f < kD; f += kThreads) pz[f] = zsh[f];
 }
 
-// s_init = s0 + sum_seg part_s[seg] (segments summed in order: deterministic).
-__global__ void prefix_reduce_kernel(const float *__restrict__ part_s,
-                                     const float *__restrict__ part_z,
-                                     const float *__restrict__ s0,
-                                     const float *__restrict__ z0, int64_t BH,
-                                     int64_t nseg, float *__restrict__ s_init,
-                                     float *__restrict__ z_init) {
-    const int64_t per = (int64_t)kD * kDV + kD;
-    const int64_t total = BH * per;
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t bh = e / per, w = e % per;
-        if (w < (int64_t)kD * kDV) {
-            float acc = s0 ? s0[bh * kD * kDV + w] : 0.f;
-            const float *p = part_s + bh * nseg * kD * kDV + w;
-            for (int64_t sg = 0; sg < nseg; ++sg) acc += p[sg * kD * kDV];
-            s_init[bh * kD * kDV + w] = acc;
-        } else {
-            const int64_t f = w - (int64_t)kD * kDV;
-            float acc = z0 ? z0[bh * kD + f] : 0.f;
-            const float *p = part_z + bh * nseg * kD + f;
-            for (int64_t sg = 0; sg < nseg; ++sg) acc += p[sg * kD];
-            z_init[bh * kD + f] = acc;
-        }
-    }
-}
-
 __global__ void state_copy_kernel(const float *__restrict__ s0,
                                   const float *__restrict__ z0, float *s_out,
                                   float *z_out, int64_t BH, int64_t D) {
@@ -236,11 +222,12 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, la_dtype dt, cudaStream_t 
         prefill_simt_kernel<__nv_bfloat16><<<(unsigned)BH, kThreads, 0, st>>>(
             (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k,
             (const __nv_bfloat16 *)a.v, a.s0, a.z0, (__nv_bfloat16 *)a.y, a.s_out,
-            a.z_out, a.N, a.eps, a.left_pad, a.H, a.status, a.gamma);
+            a.z_out, a.N, a.eps, a.left_pad, a.H, a.status, a.gamma, a.part_s, a.part_z, a.nseg);
     else
         prefill_simt_kernel<float><<<(unsigned)BH, kThreads, 0, st>>>(
             (const float *)a.q, (const float *)a.k, (const float *)a.v, a.s0, a.z0,
-            (float *)a.y, a.s_out, a.z_out, a.N, a.eps, a.left_pad, a.H, a.status, a.gamma);
+            (float *)a.y, a.s_out, a.z_out, a.N, a.eps, a.left_pad, a.H, a.status, a.gamma, a.part_s,
+            a.part_z, a.nseg);
     return cudaGetLastError();
 }
 
@@ -255,14 +242,6 @@ cudaError_t launch_prefix_partials_simt(const PrefixArgs &a, la_dtype dt, cudaSt
         prefix_partial_simt_kernel<float><<<grid, kThreads, 0, st>>>(
             (const float *)a.k_e, (const float *)a.v_e, a.M, a.seg_len, a.nseg,
             a.part_s, a.part_z, a.left_pad, a.H, a.N);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_prefix_reduce(const PrefixArgs &a, cudaStream_t st) {
-    const int64_t BH = a.B * a.H;
-    const int64_t total = BH * ((int64_t)kD * kDV + kD);
-    prefix_reduce_kernel<<<grid_for(total, 256), 256, 0, st>>>(
-        a.part_s, a.part_z, a.s0, a.z0, BH, a.nseg, a.s_init, a.z_init);
     return cudaGetLastError();
 }
 

@@ -227,6 +227,24 @@ static __device__ __noinline__ bool p_block(uint32_t tsrc, uint32_t tdst, int pp
     return true;
 }
 
+// r[j] += sum over the nseg segments, in order, of part[seg * seg_stride +
+// (32 G + j) * stride]: the prefix partial states (internal compact rows) of
+// feature group G, for one value column (or z').  The 32 reads of a segment
+// are issued together.
+template <int G>
+__device__ __forceinline__ void add_partials(const float *part, int64_t stride, int64_t seg_stride, int nseg,
+                                             uint32_t (&r)[32]) {
+#pragma unroll 1
+    for (int sg = 0; sg < nseg; ++sg) {
+        const float *p = part + sg * seg_stride + (32 * G) * stride;
+        float a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) a[j] = __ldcg(p + j * stride);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) + a[j]);
+    }
+}
+
 // Image of one head's final [273][64] fp32 state in shared memory, written
 // out with a single bulk copy once the last update has completed (the
 // feature-operand buffers it overlays are free by then).
@@ -257,7 +275,7 @@ enum { TR_TMA = 0, TR_MMA, TR_GEN, TR_EPI, TR_CONV };
 // writes gamma^(L-1-t) Phi'_K (scaled key features), the intra-chunk kernel
 // entries carry gamma^(i-j), and the state is multiplied by gamma^L in TMEM
 // before each update.
-template <bool kPad, bool kDecay, bool kCompact = false>
+template <bool kPad, bool kDecay, bool kCompact = false, bool kPrefix = false>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty,
@@ -265,7 +283,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                   const float *__restrict__ z0, const int32_t *__restrict__ left_pad,
                   const float *__restrict__ gamma, int64_t H,
                   float *__restrict__ s_out, float *__restrict__ z_out, int N, float eps,
-                  unsigned *status) {
+                  unsigned *status, const float *__restrict__ part_s, const float *__restrict__ part_z,
+                  int nseg) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -381,6 +400,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 compact_io_initial_group<G>(col0, stride, r, std::make_integer_sequence<int, 32>{});
             else
                 compact_initial_group<G>(col0, stride, r, std::make_integer_sequence<int, 32>{});
+            if constexpr (kPrefix) {
+                // + the prefix segments' partial states (internal compact rows), in order
+                const float *p = zrow ? part_z + bh * nseg * kNFeat : part_s + bh * nseg * kNFeat * kDV + d;
+                add_partials<G>(p, stride, zrow ? kNFeat : kNFeat * kDV, nseg, r);
+            }
             __syncwarp();
             if (!zrow || lane == 0) write_sb_group(sb + kSmSb, zrow ? 64 : d, G, r);
             if constexpr (kDecay) {  // the first update starts from gamma^L0 s0
@@ -841,23 +865,44 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(prefill_tc_kernel<false, false, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<false, false, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<true, false, false, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
     if (a.left_pad && a.gamma) return cudaErrorInvalidValue;  // no padded decayed variant
     if (a.compact && (a.left_pad || a.gamma)) return cudaErrorInvalidValue;  // plain prefill only
-    if (a.compact)
+    const bool prefix = a.part_s != nullptr;
+    if (prefix && (a.gamma || a.compact || a.nseg < 1 || a.nseg > 65535)) return cudaErrorInvalidValue;
+    const int nseg = (int)a.nseg;
+    if (prefix && a.left_pad)
+        prefill_tc_kernel<true, false, false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
+            tq, tk, tv, ty, a.s0, a.z0, a.left_pad, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
+            a.part_s, a.part_z, nseg);
+    else if (prefix)
+        prefill_tc_kernel<false, false, false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
+            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
+            a.part_s, a.part_z, nseg);
+    else if (a.compact)
         prefill_tc_kernel<false, false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
+            nullptr, nullptr, 0);
     else if (a.left_pad)
         prefill_tc_kernel<true, false><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, a.left_pad, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+            tq, tk, tv, ty, a.s0, a.z0, a.left_pad, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
+            nullptr, nullptr, 0);
     else if (a.gamma)
         prefill_tc_kernel<false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, nullptr, a.gamma, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+            tq, tk, tv, ty, a.s0, a.z0, nullptr, a.gamma, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
+            nullptr, nullptr, 0);
     else
         prefill_tc_kernel<false, false><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status);
+            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
+            nullptr, nullptr, 0);
     return cudaGetLastError();
 }
 

@@ -3,14 +3,17 @@
 //   s_E,seg = sum_j phi(k_e_j) v_e_j^T,   z_E,seg = sum_j phi(k_e_j)
 // ("Just read twice" reading notes, sec. 2.6: the non-causal encoder state of
 // prefix linear attention; sec. 2.8: the encoder state is accumulated first
-// and then seeds the causal scan).  A deterministic second pass adds the
-// segments in order (prefill_simt.cu), and the causal prefill starts from it.
+// and then seeds the causal scan).  Each partial is written as the kernel
+// holds it, in the internal compact rows ([160][64] values and [160] z', fp32,
+// row = compact feature); the causal prefill's set-up adds the segments to
+// its initial state in segment order (deterministic), so there is no
+// separate reduction pass.
 //
 // Same update as the causal prefill kernel: [S'^T ; z'] += [V | 1]^T Phi'_K
 // per 128-token chunk (8 MMAs of M = 128, N = 160, K = 16), with the compact
 // feature map generated one token per thread.  Splitting the prefix over
 // segments spreads the reduction over all SMs instead of lengthening each
-// (b, h) scan.  256 threads, about 108 KB of shared memory and 256 TMEM
+// (b, h) scan.  256 threads, about 111 KB of shared memory and 256 TMEM
 // columns per CTA, so two CTAs share an SM.
 #include "la_internal.h"
 #include "taylor_tc.cuh"
@@ -24,21 +27,24 @@ using namespace taylor;
 
 constexpr int kC = 128;
 constexpr int kThreads = 256;
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 
 // Shared memory map (bytes from a 1024-aligned base)
 constexpr uint32_t kSmPhiK = 0;        // MN-major B: 3 x 16K SW128
-constexpr uint32_t kSmV = 49152;       // 2 x [128][64] bf16 SW128
-constexpr uint32_t kSmOnes = 81920;    // [128][64] bf16 ones (rows 64..127 of [V | 1]^T)
-constexpr uint32_t kSmK = 98304;       // 2 x [128][16] bf16 SW32
-constexpr uint32_t kSmBar = 106496;
+constexpr uint32_t kSmV = 49152;       // 3 x [128][64] bf16 SW128
+constexpr uint32_t kSmOnes = 98304;    // [16][64] bf16 ones: rows 64..127 of [V | 1]^T for every K step
+constexpr uint32_t kSmK = 100352;      // 3 x [128][16] bf16 SW32
+constexpr uint32_t kSmBar = 112640;
 constexpr uint32_t kSmTotal = kSmBar + 256;
 constexpr uint32_t kSmAlloc = kSmTotal + 1024;
 
-enum { B_KV_FULL = 0, B_KV_EMPTY = 2, B_PHK_FULL = 4, B_PHK_EMPTY, B_S_FULL, B_COUNT };
+enum { B_KV_FULL = 0, B_KV_EMPTY = kStages, B_PHK_FULL = 2 * kStages, B_PHK_EMPTY, B_S_FULL, B_COUNT };
 constexpr uint32_t kSmTmemSlot = kSmBar + 8 * B_COUNT;
 constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
 static_assert(kSmAbort + 4 <= kSmTotal, "barrier area");
+static_assert(kSmV + kStages * 16384 <= kSmOnes && kSmOnes + 2048 <= kSmK && kSmK + kStages * 4096 <= kSmBar,
+              "shared memory map");
+static_assert(2 * (kSmAlloc + 1024) <= 233472, "two CTAs per SM");
 
 constexpr uint32_t kIdUp = idesc_bf16(128, kNFeat, true, true);  // [V | 1]^T x Phi'_K
 
@@ -78,7 +84,7 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
         tmem_alloc(sb + kSmTmemSlot, 256);
         tmem_relinquish();
     }
-    for (int i = tid; i < 16384 / 16; i += kThreads)
+    for (int i = tid; i < 2048 / 16; i += kThreads)
         st_shared_v4(sb + kSmOnes + 16 * i, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     fence_async_smem();
     tc_fence_before();
@@ -109,18 +115,22 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
         // ================= MMA issuer: [S'^T ; z'] += [V | 1]^T Phi'_K =================
         if (lane == 0) {
             const uint64_t dPhiK = smem_desc(sb + kSmPhiK, 16384, 1024, kSw128);
-            const uint64_t dV0 = smem_desc(sb + kSmV, kSmOnes - kSmV, 1024, kSw128);
             bool ok = true;
             for (int c = 0; c < n; ++c) {
                 const int st = c % kStages;
-                const uint64_t dV = dV0 + (uint64_t)(st * (16384 >> 4)) - ((uint64_t)(st * (16384 >> 4)) << 16);
                 ok = mbar_wait(bar(B_PHK_FULL), (uint32_t)c & 1u, abort, status) &&
                      mbar_wait(bar(B_KV_FULL + st), (uint32_t)(c / kStages) & 1u, abort, status);
                 if (!ok) break;
                 tc_fence_after();
+                // A = [V | 1]^T, MN-major: K step s reads value rows 0..63 from its
+                // 16 tokens of the V stage and rows 64..127 from the one 2 KB ones
+                // block (the leading byte offset is the distance between the two)
 #pragma unroll
-                for (int s = 0; s < 8; ++s)
-                    mma_bf16(tmem, dV + s * (2048 >> 4), dPhiK + s * (2048 >> 4), kIdUp, (c > 0 || s > 0));
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t va = kSmV + (uint32_t)st * 16384u + (uint32_t)s * 2048u;
+                    mma_bf16(tmem, smem_desc(sb + va, kSmOnes - va, 1024, kSw128), dPhiK + s * (2048 >> 4), kIdUp,
+                             (c > 0 || s > 0));
+                }
                 mma_commit(bar(B_PHK_EMPTY));
                 mma_commit(bar(B_KV_EMPTY + st));
             }
@@ -144,19 +154,33 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_PHK_FULL));
         }
-        // ---- partial state of this segment in the ABI layout (value rows d: lanes
-        // 0..63 of warps 4, 5; the z' row: lane 64, warp 6)
+        // ---- partial state of this segment in the internal compact rows (value
+        // d: lanes 0..63 of warps 4, 5, entry (F, d) at [F * 64 + d]; z': lane
+        // 64, warp 6, entry F at [F]).  An empty segment writes zeros.
         if (warp < 7) {
             const int w = warp - 4;
             const bool zrow = (w == 2);
-            const bool ok = mbar_wait(bar(B_S_FULL), 0, abort, status);
+            const bool ok = n == 0 || mbar_wait(bar(B_S_FULL), 0, abort, status);
             __syncwarp();
             tc_fence_after();
-            if (ok && n > 0) {
+            if (ok) {
                 const int64_t slot = bh * nseg + seg;
-                final_groups<false, 0>(tmem + ((uint32_t)(32 * w) << 16), 32 * w + lane, zrow, lane, nullptr, 0u,
-                                       part_s + slot * kD * kDV, nullptr, part_z + slot * kD, 1.f,
-                                       std::make_integer_sequence<int, kNFeat / 32>{});
+                float *dst = zrow ? part_z + slot * kNFeat : part_s + slot * kNFeat * kDV + 32 * w + lane;
+                const int64_t stride = zrow ? 1 : kDV;
+#pragma unroll 1
+                for (int G = 0; G < kNFeat / 32; ++G) {
+                    uint32_t r[32];
+                    if (n > 0) {
+                        tmem_load32_sync(tmem + ((uint32_t)(32 * w) << 16) + 32 * G, r);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;
+                    }
+                    if (!zrow || lane == 0) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) __stcg(dst + (32 * G + j) * stride, __uint_as_float(r[j]));
+                    }
+                }
             }
         }
     }

@@ -41,7 +41,7 @@ def test_noalloc_rejects_problems_larger_than_its_buffer():
     never-dereferenced pointers; no GPU needed)."""
     build.build()
     lib = binding.load_library()
-    B, H, M = 16, 16, 16384
+    B, H, M = 64, 16, 16384
     assert lib.la_prefix_workspace_size(B, H, M) > lib.la_noalloc_scratch_bytes()
     p = [ctypes.c_void_p(0x7F0000000000 + i * (1 << 36)) for i in range(10)]
     rc = lib.la_prefix_prefill_noalloc(p[0], p[1], p[2], p[3], p[4], M, p[5], p[6], p[7], p[8],
