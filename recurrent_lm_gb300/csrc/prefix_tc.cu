@@ -38,7 +38,12 @@ constexpr uint32_t kSmBar = 112640;
 constexpr uint32_t kSmTotal = kSmBar + 256;
 constexpr uint32_t kSmAlloc = kSmTotal + 1024;
 
-enum { B_KV_FULL = 0, B_KV_EMPTY = kStages, B_PHK_FULL = 2 * kStages, B_PHK_EMPTY, B_S_FULL, B_COUNT };
+// Phi'_K is produced and consumed in two halves of 64 tokens (K steps 0..3 and
+// 4..7), each with its own full / empty barrier, so that the features of one
+// half of chunk c + 1 are generated while the update reads the other half of
+// chunk c.
+enum { B_KV_FULL = 0, B_KV_EMPTY = kStages, B_PHK_FULL = 2 * kStages, B_PHK_EMPTY = 2 * kStages + 2,
+       B_S_FULL = 2 * kStages + 4, B_COUNT };
 constexpr uint32_t kSmTmemSlot = kSmBar + 8 * B_COUNT;
 constexpr uint32_t kSmAbort = kSmTmemSlot + 4;
 static_assert(kSmAbort + 4 <= kSmTotal, "barrier area");
@@ -47,6 +52,20 @@ static_assert(kSmV + kStages * 16384 <= kSmOnes && kSmOnes + 2048 <= kSmK && kSm
 static_assert(2 * (kSmAlloc + 1024) <= 233472, "two CTAs per SM");
 
 constexpr uint32_t kIdUp = idesc_bf16(128, kNFeat, true, true);  // [V | 1]^T x Phi'_K
+
+// Optional per-role timeline of CTA (0, 0) (compile with -DLA_TRACE): SM clock
+// offsets from kernel entry for events of each role and chunk.
+#ifdef LA_TRACE
+constexpr int kPTraceChunks = 256;
+__device__ uint32_t g_ptrace[3][kPTraceChunks][4];
+#define LA_PTR(role, c, ev)                                                              \
+    do {                                                                                 \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && (c) < kPTraceChunks)                   \
+            g_ptrace[role][c][ev] = (uint32_t)(clock64() - t_start);                     \
+    } while (0)
+#else
+#define LA_PTR(role, c, ev) do { } while (0)
+#endif
 
 __global__ void __launch_bounds__(kThreads, 2)
 prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -63,6 +82,9 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t bh = blockIdx.x;
     const int seg = blockIdx.y;
+#ifdef LA_TRACE
+    const long long t_start = clock64();
+#endif
     const int j0 = seg * seg_len;
     const int j1 = min(M, j0 + seg_len);
     const int n = (j1 - j0 + kC - 1) / kC;
@@ -74,8 +96,10 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
             mbar_init(bar(B_KV_FULL + s), 1);
             mbar_init(bar(B_KV_EMPTY + s), 1 + 4);
         }
-        mbar_init(bar(B_PHK_FULL), 4);
-        mbar_init(bar(B_PHK_EMPTY), 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(B_PHK_FULL + h), 2);  // the two generation warps of the half
+            mbar_init(bar(B_PHK_EMPTY + h), 1);
+        }
         mbar_init(bar(B_S_FULL), 1);
         *abort = 0;
         mbar_init_fence();
@@ -100,8 +124,10 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
             int issued = 0;
             for (int c = 0; c < n; ++c) {
                 const int st = c % kStages;
+                LA_PTR(0, c, 0);
                 if (!mbar_wait(bar(B_KV_EMPTY + st), ((uint32_t)(c / kStages) & 1u) ^ 1u, abort, status))
                     break;
+                LA_PTR(0, c, 1);
                 mbar_expect_tx(bar(B_KV_FULL + st), kC * 16 * 2 + kC * 64 * 2);
                 tma_load_3d(sb + kSmK + st * 4096, &tk, bar(B_KV_FULL + st), 0, j0 + c * kC, (int)bh);
                 tma_load_3d(sb + kSmV + st * 16384, &tv, bar(B_KV_FULL + st), 0, j0 + c * kC, (int)bh);
@@ -116,43 +142,50 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
         if (lane == 0) {
             const uint64_t dPhiK = smem_desc(sb + kSmPhiK, 16384, 1024, kSw128);
             bool ok = true;
-            for (int c = 0; c < n; ++c) {
+            for (int c = 0; c < n && ok; ++c) {
                 const int st = c % kStages;
-                ok = mbar_wait(bar(B_PHK_FULL), (uint32_t)c & 1u, abort, status) &&
-                     mbar_wait(bar(B_KV_FULL + st), (uint32_t)(c / kStages) & 1u, abort, status);
-                if (!ok) break;
-                tc_fence_after();
-                // A = [V | 1]^T, MN-major: K step s reads value rows 0..63 from its
-                // 16 tokens of the V stage and rows 64..127 from the one 2 KB ones
-                // block (the leading byte offset is the distance between the two)
+                ok = mbar_wait(bar(B_KV_FULL + st), (uint32_t)(c / kStages) & 1u, abort, status);
+                for (int h = 0; h < 2 && ok; ++h) {
+                    if (!(ok = mbar_wait(bar(B_PHK_FULL + h), (uint32_t)c & 1u, abort, status))) break;
+                    if (h == 0) LA_PTR(1, c, 0);
+                    tc_fence_after();
+                    // A = [V | 1]^T, MN-major: K step s reads value rows 0..63 from its
+                    // 16 tokens of the V stage and rows 64..127 from the one 2 KB ones
+                    // block (the leading byte offset is the distance between the two)
 #pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t va = kSmV + (uint32_t)st * 16384u + (uint32_t)s * 2048u;
-                    mma_bf16(tmem, smem_desc(sb + va, kSmOnes - va, 1024, kSw128), dPhiK + s * (2048 >> 4), kIdUp,
-                             (c > 0 || s > 0));
+                    for (int s = 4 * h; s < 4 * h + 4; ++s) {
+                        const uint32_t va = kSmV + (uint32_t)st * 16384u + (uint32_t)s * 2048u;
+                        mma_bf16(tmem, smem_desc(sb + va, kSmOnes - va, 1024, kSw128), dPhiK + s * (2048 >> 4),
+                                 kIdUp, (c > 0 || s > 0));
+                    }
+                    mma_commit(bar(B_PHK_EMPTY + h));
                 }
-                mma_commit(bar(B_PHK_EMPTY));
-                mma_commit(bar(B_KV_EMPTY + st));
+                if (ok) mma_commit(bar(B_KV_EMPTY + st));
+                LA_PTR(1, c, 1);
             }
             mma_commit(bar(B_S_FULL));  // also covers an early exit: every issued MMA completes first
         }
     } else if (warp >= 4) {
         // ================= feature generation (one token per thread) =================
         const int t = tid - 128;
+        const int h = t >> 6;  // the half of the Phi'_K tile this warp writes
         for (int c = 0; c < n; ++c) {
             const int st = c % kStages;
             if (!mbar_wait(bar(B_KV_FULL + st), (uint32_t)(c / kStages) & 1u, abort, status)) break;
+            if (tid == 128) LA_PTR(2, c, 0);
             uint4 klo, khi;
             load_row16_raw(sb + kSmK + st * 4096, t, klo, khi);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_KV_EMPTY + st));
-            if (!mbar_wait(bar(B_PHK_EMPTY), ((uint32_t)c & 1u) ^ 1u, abort, status)) break;
+            if (!mbar_wait(bar(B_PHK_EMPTY + h), ((uint32_t)c & 1u) ^ 1u, abort, status)) break;
+            if (tid == 128) LA_PTR(2, c, 1);
             // outside this segment, or left padding: no contribution
             const bool pad = j0 + c * kC + t >= j1 || j0 + c * kC + t < pe;
             emit_features<true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PHK_FULL));
+            if (lane == 0) mbar_arrive(bar(B_PHK_FULL + h));
+            if (tid == 128) LA_PTR(2, c, 2);
         }
         // ---- partial state of this segment in the internal compact rows (value
         // d: lanes 0..63 of warps 4, 5, entry (F, d) at [F * 64 + d]; z': lane
@@ -195,6 +228,13 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
 }
 
 }  // namespace
+
+#ifdef LA_TRACE
+extern "C" LA_API int la_debug_prefix_trace(void *host, size_t bytes) {
+    if (bytes > sizeof(g_ptrace)) bytes = sizeof(g_ptrace);
+    return (int)cudaMemcpyFromSymbol(host, g_ptrace, bytes);
+}
+#endif
 
 cudaError_t launch_prefix_partials_tc(const PrefixArgs &a, cudaStream_t st) {
     const int64_t BH = a.B * a.H;
