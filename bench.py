@@ -657,7 +657,7 @@ def main():
             "tokens_per_s": W * r["B"] * r["N"] / t, "achieved_tflops": fl / t / 1e12,
             "tc_frac": fl / t / 1e12 / pk["bf16_tflops"], "hbm_gbs": by / t / 1e9,
             "hbm_frac": by / t / 1e9 / pk["hbm_gbs"]}
-        launches += 3 * max(1, args.steps // 2)
+        launches += 2 * max(1, args.steps // 2)
     if "prefix_padded" in res:
         r = res["prefix_padded"]
         t = r["ms"] / 1e3
@@ -665,7 +665,7 @@ def main():
             "workload": inputs.WORKLOADS[4].name + "-leftpad-uniform0toM", "ms_per_call": r["ms"],
             "tokens_per_s": W * r["B"] * r["N"] / t,
             "valid_tokens_per_s": W * r["valid_tokens"] / t}
-        launches += 3 * max(1, args.steps // 2)
+        launches += 2 * max(1, args.steps // 2)
     if "jrt_prompt" in res:
         r = res["jrt_prompt"]
         t = r["ms"] / 1e3
@@ -721,8 +721,8 @@ def main():
                                          "each step (larger than L2); us_per_step is per layer-step")
         launches += r["steps_per_graph"] * max(1, args.steps // 4)
     line["gpu_launches"] = launches
-    line["gpu_launches_note"] = ("prefill leg: 1 kernel per step; prefix leg: 3 per call; "
-                                 "decode leg: 1 per decode step")
+    line["gpu_launches_note"] = ("prefill leg: 1 kernel per step; prefix legs: 2 per call; "
+                                 "decode legs: 1 per decode step (per layer-step in decode_compact)")
     line["finite_outputs"] = pre["finite"]
     if dist.rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(args.cpu_sample_rows)
