@@ -258,13 +258,18 @@ def leg_prefill(la, args, dist, dev, clocks):
     y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
     s = torch.empty_like(s0)
     z = torch.empty_like(z0)
+    # la_prefill_ws: the workspace lets the last wave's heads run split
+    split = not args.no_split
+    need = la.load_library().la_prefill_workspace_size(B, H, N, 16, la.binding.LA_DTYPE_BF16)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev) if split else None
 
     def step():
-        la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z)
+        la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z, workspace=ws, split=split)
 
     ms = time_loop(step, args.steps, args.warmup, dist)
     la.check_device_status()
-    out = {"ms": ms, "B": B, "H": H, "N": N,
+    r, n1 = la.prefill_split_info(B, H, N) if split else (0, 0)
+    out = {"ms": ms, "B": B, "H": H, "N": N, "split_heads": r, "split_chunk": n1,
            "finite": bool(torch.isfinite(y[:, :, -1].float()).all().item())}
     if not args.no_e2e:
         out["e2e"] = e2e_prefill(la, args, dist, q, k, v, s0, z0)
@@ -559,6 +564,8 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-split", action="store_true",
+                    help="time la_prefill without the workspace (no split heads in the last wave)")
     ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_compact", "prefix"],
                     help="run one small case for an ncu capture and exit (no timing)")
     args = ap.parse_args()
@@ -628,6 +635,7 @@ def main():
                    "N": pre["N"], "d_feat": 16, "d_v": 64, "D": 273, "s0_tokens": 4096,
                    "global_batch": W * pre["B"], "seq_len": pre["N"],
                    "parallelism": f"independent (b,h) shards x{W}",
+                   "split_heads": pre["split_heads"], "split_chunk": pre["split_chunk"],
                    "l2": "inputs larger than L2 (2.1 GB of q,k,v per step)"},
         "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": pk["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved_tf / pk["bf16_tflops"],

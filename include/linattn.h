@@ -105,6 +105,40 @@ LA_API la_status la_prefill(const void *q, const void *k, const void *v,
                      la_dtype dtype, float eps, la_stream_t stream);
 
 /*
+ * la_prefill_ws -- la_prefill with a caller workspace that lets the bf16
+ * tensor-core path balance its last wave of heads.
+ *
+ * The kernel runs one CTA per (b, h) on each SM, so B*H heads take
+ * ceil(B*H / SMs) waves and the last wave leaves SMs idle.  With a workspace,
+ * the heads of the last wave are each split into two pieces along the
+ * sequence: the first piece runs on an otherwise idle SM early and hands its
+ * state to the second through the workspace (the blockwise state carry of the
+ * BASED reading notes, sec. 2.5, across two CTAs).  The results are those of
+ * la_prefill up to fp32 rounding order in the handed-over state; they are
+ * reproducible on a given device (the split depends on its SM count).
+ *
+ *   workspace: DEVICE buffer of at least la_prefill_workspace_size(B, H, N,
+ *   d_feat, dtype) bytes, 256-byte aligned, owned by the caller, not read
+ *   before written.  It must not be used by two calls whose work overlaps on
+ *   the GPU.  NULL, or too small, runs exactly la_prefill.
+ * All other arguments, layouts and errors are those of la_prefill (padding and
+ * decay have no workspace form).  la_prefill_workspace_size returns 0 where no
+ * split is possible (fp32 activations, d_feat != 16).
+ */
+LA_API size_t la_prefill_workspace_size(int64_t B, int64_t H, int64_t N, int d_feat, la_dtype dtype);
+/* The split la_prefill_ws (and the prefix call) make on the current device for
+ * these sizes: *split_heads heads (the last ones) run as the chunks [0,
+ * *split_chunk) and [*split_chunk, ceil(N/128)); 0 and 0 when none. */
+LA_API la_status la_prefill_split_info(int64_t B, int64_t H, int64_t N, int *split_heads,
+                                       int *split_chunk);
+LA_API la_status la_prefill_ws(const void *q, const void *k, const void *v,
+                               const float *s0, const float *z0,
+                               void *y, float *s_out, float *z_out,
+                               void *workspace, size_t workspace_bytes,
+                               int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                               la_dtype dtype, float eps, la_stream_t stream);
+
+/*
  * la_prefill_host -- la_prefill for activations and states that live in host
  * memory: the same computation, with the host <-> device copies inside the
  * call and overlapped with the kernels.
@@ -159,9 +193,13 @@ LA_API size_t la_prefix_workspace_size(int64_t B, int64_t H, int64_t M);
  *
  *   k_e in [B][H][M][16] dtype, v_e in [B][H][M][64] dtype (ignored if M == 0)
  *   0 <= M <= N, else LA_ERR_INVALID_ARG.
- *   workspace: device buffer of at least la_prefix_workspace_size(B, H, M)
- *   bytes, 256-byte aligned, owned by the caller, not read before it is
- *   written; it may be reused once the call's work on `stream` is done.
+ *   workspace: device buffer of la_prefix_workspace_size(B, H, M) bytes,
+ *   256-byte aligned, owned by the caller, not read before it is written; it
+ *   may be reused once the call's work on `stream` is done.  That size
+ *   includes a region through which the prefill hands state between the two
+ *   pieces of a split head (see la_prefill_ws); a smaller workspace that
+ *   still holds the prefix partial states (B*H*nseg * 70,980 bytes, rounded
+ *   up; see la_prefix_prefill_noalloc) runs without split heads.
  * Other arguments as for la_prefill.
  */
 LA_API la_status la_prefix_prefill(const void *q, const void *k, const void *v,
@@ -364,10 +402,12 @@ LA_API la_status la_decode_step_compact(const void *q, const void *k, const void
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before capturing the stream into a CUDA graph.
  *   - Problems with la_prefix_workspace_size(B, H, M) larger than the buffer
- *     return LA_ERR_SCRATCH_TOO_SMALL before any work is queued.  The
- *     workspace holds B*H*nseg partial states of 70,980 bytes, with nseg =
+ *     return LA_ERR_SCRATCH_TOO_SMALL before any work is queued.  The call
+ *     needs B*H*nseg partial states of 70,980 bytes, with nseg =
  *     min(16, ceil(256 / (B*H)), ceil(M / 128)) prefix segments (fewer once
  *     their length is rounded up to 128 tokens), so B*H*nseg <= 472 fits.
+ *     When the buffer also holds la_prefix_workspace_size(B, H, M) bytes, the
+ *     prefill splits its last wave of heads as la_prefill_ws does.
  *   - Every call on a device shares the buffer, and the buffer keeps the last
  *     call's contents.  Nothing in it needs to start at zero (each call
  *     writes every part it reads).  Calls whose work overlaps on the GPU (two

@@ -52,6 +52,11 @@ SIGNATURES = {
                                   _I, _F, _VP]),
     "la_prefix_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "la_prefill_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _I]),
+    "la_prefill_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _I]),
+    "la_prefill_split_info": (_I, [_I64, _I64, _I64, ctypes.POINTER(ctypes.c_int),
+                                   ctypes.POINTER(ctypes.c_int)]),
+    "la_prefill_ws": (_I, [_VP, _VP, _VP, _FP, _FP, _VP, _FP, _FP, _VP, _SZ, _I64, _I64, _I64, _I, _I,
+                           _I, _F, _VP]),
     "la_prefill_host": (_I, [_VP, _VP, _VP, _FP, _FP, _VP, _FP, _FP, _VP, _SZ, _I64, _I64, _I64,
                              _I, _I, _I, _F, _VP]),
     "la_prefix_prefill": (_I, [_VP, _VP, _VP, _VP, _VP, _I64, _FP, _FP, _VP, _FP, _FP, _VP,
@@ -149,12 +154,16 @@ def _need_pad(left_pad, B):
 
 
 def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
-            z_out=None, want_state: bool = True, stream=None, left_pad=None, gamma=None):
-    """Causal prefill (la_prefill).  q,k [B,H,N,16], v [B,H,N,64] (bf16 or fp32,
-    CUDA, contiguous); s0 [B,H,273,64], z0 [B,H,273] fp32 or None.
+            z_out=None, want_state: bool = True, stream=None, left_pad=None, gamma=None,
+            workspace=None, split: bool = True):
+    """Causal prefill.  q,k [B,H,N,16], v [B,H,N,64] (bf16 or fp32, CUDA,
+    contiguous); s0 [B,H,273,64], z0 [B,H,273] fp32 or None.
     left_pad: CUDA int32 [B] counts of leading padding positions per batch row
     (la_prefill_padded), or None.  gamma: CUDA fp32 [H] per-head decay in
     [0, 1] (la_prefill_decay), or None; not combined with left_pad.
+    Without either, the call is la_prefill_ws with ``workspace`` (a CUDA uint8
+    tensor of la_prefill_workspace_size bytes; allocated here if None), or
+    la_prefill when split is False.
     Returns (y, s_out, z_out); the states are None when want_state is False."""
     lib = load_library()
     B, H, N, dk = q.shape
@@ -187,13 +196,33 @@ def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
                                     _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, dk, D_V, _dt(q),
                                     float(eps), _stream(stream)))
     elif left_pad is None:
-        _raise(lib.la_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
-                              _ptr(z_out), B, H, N, dk, D_V, _dt(q), float(eps), _stream(stream)))
+        # la_prefill_ws with a workspace from torch's caching allocator (it
+        # balances the last wave of heads on the bf16 path); la_prefill when
+        # the call has no workspace form
+        need = int(lib.la_prefill_workspace_size(B, H, N, dk, _dt(q))) if split else 0
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            _keep_for(workspace, stream)
+        if workspace is not None:
+            _need(workspace, "workspace", (workspace.numel(),), torch.uint8)
+            _raise(lib.la_prefill_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
+                                     _ptr(z_out), _ptr(workspace), workspace.numel(), B, H, N, dk, D_V,
+                                     _dt(q), float(eps), _stream(stream)))
+        else:
+            _raise(lib.la_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(y), _ptr(s_out),
+                                  _ptr(z_out), B, H, N, dk, D_V, _dt(q), float(eps), _stream(stream)))
     else:
         _raise(lib.la_prefill_padded(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(left_pad),
                                      _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, dk, D_V, _dt(q),
                                      float(eps), _stream(stream)))
     return y, s_out, z_out
+
+
+def prefill_split_info(B: int, H: int, N: int):
+    """(split_heads, split_chunk) that la_prefill_ws chooses on the current device."""
+    r, c = ctypes.c_int(0), ctypes.c_int(0)
+    _raise(load_library().la_prefill_split_info(B, H, N, ctypes.byref(r), ctypes.byref(c)))
+    return r.value, c.value
 
 
 def _need_host(t: torch.Tensor, name: str, shape, dtype):

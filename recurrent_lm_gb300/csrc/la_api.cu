@@ -1,6 +1,7 @@
 // C-ABI layer of liblinattn.so: argument validation on the host, workspace
 // carving, and dispatch to the kernel launchers.  Nothing is launched unless
 // every argument check passes.  See include/linattn.h for the contract.
+#include <atomic>
 #include <mutex>
 
 #include "la_internal.h"
@@ -16,7 +17,9 @@ __device__ unsigned g_la_status = 0;
 constexpr int kMaxDevices = 64;
 unsigned *g_status_ptr[kMaxDevices] = {};
 int g_cc[kMaxDevices] = {};  // major*10+minor, 0 = not queried yet
+int g_sms[kMaxDevices] = {};  // multiprocessor count
 std::mutex g_mu;
+std::atomic<unsigned long long> g_call_id{1};  // flag value of split heads' state hand-over
 
 // Per-device set-up: compute capability and the status word's address.
 la_status device_setup(int *dev_out, unsigned **status) {
@@ -26,9 +29,12 @@ la_status device_setup(int *dev_out, unsigned **status) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_cc[dev] == 0) {
         int major = 0, minor = 0;
+        int sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return LA_ERR_CUDA;
+        g_sms[dev] = sms;
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_la_status) != cudaSuccess) return LA_ERR_CUDA;
         g_status_ptr[dev] = static_cast<unsigned *>(p);
@@ -82,11 +88,59 @@ size_t esize(la_dtype dt) { return dt == LA_DTYPE_BF16 ? 2 : 4; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Split heads of the bf16 prefill.  One CTA per head and per SM, so B*H heads
+// run in W = ceil(B*H / SMs) waves, the last with r heads and SMs - r idle
+// SMs.  The r heads of the last wave are split at chunk n1 into a first piece
+// (chunks [0, n1)) and a second piece (the rest), and the block order is
+//   r whole heads, r first pieces, the other whole heads, r second pieces.
+// So r SMs run whole heads and then a second piece, and the other SMs run
+// k = ceil(r / (SMs - r)) first pieces before their whole heads; the first
+// pieces are done long before the second pieces start (blocks are dispatched
+// in order).  n1 balances the two kinds of SM, counting f = 10 chunk times of
+// fixed cost per CTA (set-up and final state): n - n1 + f = k (n1 + f).
+struct SplitPlan {
+    int r = 0, n1 = 0;
+};
+SplitPlan split_plan(int64_t BH, int64_t N, int sms) {
+    SplitPlan p;
+    const int64_t n = (N + 127) / 128;
+    if (sms < 2 || n < 32) return p;
+    const int64_t W = (BH + sms - 1) / sms;
+    if (W < 2) return p;
+    const int64_t r = BH - (W - 1) * sms;
+    if (r <= 0 || r >= sms) return p;
+    const int64_t k = (r + (sms - r) - 1) / (sms - r);
+    const int64_t f = 10;
+    const int64_t n2 = (k * n + (k - 1) * f) / (k + 1);
+    const int64_t n1 = n - n2;
+    if (n1 < 4 || n2 < 4) return p;
+    p.r = (int)r;
+    p.n1 = (int)n1;
+    return p;
+}
+
+// Transfer slots and flag words of the split heads, for up to B*H heads.
+size_t xfer_bytes(int64_t BH) { return align256(sizeof(float) * BH * la::kXferFloats); }
+size_t xflag_bytes(int64_t BH) { return align256(sizeof(unsigned long long) * BH); }
+
+// Fills the split fields of `a` for a bf16 prefill when a workspace region
+// (xfer: xfer_bytes(B*H), then xflag_bytes(B*H)) is available.
+void plan_split(la::PrefillArgs &a, int dev, char *xfer_region) {
+    if (!xfer_region) return;
+    const SplitPlan p = split_plan(a.B * a.H, a.N, g_sms[dev]);
+    if (p.r == 0) return;
+    a.split_r = p.r;
+    a.split_n1 = p.n1;
+    a.xfer = reinterpret_cast<float *>(xfer_region);
+    a.xflag = reinterpret_cast<unsigned long long *>(xfer_region + xfer_bytes(a.B * a.H));
+    a.call_id = g_call_id.fetch_add(1);
+}
+
 // Workspace of the prefix call: the per-segment partial states, sized for
 // the 273-row layout of the fp32 path (the bf16 path uses the first 160 rows'
 // worth of each part).
 struct PrefixLayout {
-    size_t part_s, part_z, total;
+    size_t part_s, part_z, base_total, xfer, total;  // base_total: without the split heads' region
 };
 
 PrefixLayout prefix_layout(int64_t BH, int64_t M) {
@@ -96,6 +150,8 @@ PrefixLayout prefix_layout(int64_t BH, int64_t M) {
     size_t off = 0;
     L.part_s = off; off = align256(off + sizeof(float) * BH * nseg * kD * kDV);
     L.part_z = off; off = align256(off + sizeof(float) * BH * nseg * kD);
+    L.base_total = off;
+    L.xfer = off;   off += xfer_bytes(BH) + xflag_bytes(BH);  // split heads of the prefill (optional)
     L.total = off;
     return L;
 }
@@ -146,7 +202,7 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
                        const float *z0, const int32_t *left_pad, void *y, float *s_out,
                        float *z_out, int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
                        la_dtype dtype, float eps, la_stream_t stream, const float *gamma = nullptr,
-                       bool compact = false) {
+                       bool compact = false, void *workspace = nullptr, size_t workspace_bytes = 0) {
     la_status st = check_common(B, H, N, d_feat, d_v, dtype);
     if (st != LA_OK) return st;
     // padding and decay exist for d' = 16 only
@@ -167,6 +223,14 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
     const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * D * kDV},
                          {z_out, sizeof(float) * BH * D}};
     if (any_overlap(in, 5, out, 3)) return LA_ERR_INVALID_ARG;
+    if (workspace) {
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return LA_ERR_MISALIGNED;
+        const Range ws{workspace, workspace_bytes};
+        for (const Range &r : in)
+            if (overlaps(ws, r)) return LA_ERR_INVALID_ARG;
+        for (const Range &r : out)
+            if (overlaps(ws, r)) return LA_ERR_INVALID_ARG;
+    }
     if ((left_pad && !aligned4(left_pad)) || (gamma && !aligned4(gamma))) return LA_ERR_MISALIGNED;
     for (const Range &o : out)
         if (overlaps({left_pad, sizeof(int32_t) * B}, o) || overlaps({gamma, sizeof(float) * H}, o))
@@ -176,6 +240,10 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
     la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad, gamma};
     a.compact = compact;
+    // split heads on the bf16 tensor-core path, given room for the hand-over
+    if (workspace && dtype == LA_DTYPE_BF16 && d_feat == kDFeat && !gamma &&
+        workspace_bytes >= xfer_bytes(BH) + xflag_bytes(BH))
+        plan_split(a, dev, static_cast<char *>(workspace));
     return to_status(run_prefill(a, dtype, reinterpret_cast<cudaStream_t>(stream), d_feat));
 }
 
@@ -196,7 +264,7 @@ la_status prefix_impl(const void *q, const void *k, const void *v, const void *k
     if (!q || !k || !v || !y || !k_e || !v_e || !workspace) return LA_ERR_INVALID_ARG;
     const int64_t BH = B * H;
     const PrefixLayout L = prefix_layout(BH, M);
-    if (workspace_bytes < L.total) return LA_ERR_INVALID_ARG;
+    if (workspace_bytes < L.base_total) return LA_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, k_e, v_e, s0, z0, y, s_out, z_out};
     for (const void *p : ptrs)
         if (p && !aligned16(p)) return LA_ERR_MISALIGNED;
@@ -207,7 +275,7 @@ la_status prefix_impl(const void *q, const void *k, const void *v, const void *k
                         {v_e, es * BH * M * kDV}, {s0, sizeof(float) * BH * kD * kDV},
                         {z0, sizeof(float) * BH * kD}};
     const Range out[] = {{y, es * BH * N * kDV}, {s_out, sizeof(float) * BH * kD * kDV},
-                         {z_out, sizeof(float) * BH * kD}, {workspace, L.total}};
+                         {z_out, sizeof(float) * BH * kD}, {workspace, workspace_bytes}};
     if (any_overlap(in, 7, out, 4)) return LA_ERR_INVALID_ARG;
     if (left_pad) {
         if (!aligned4(left_pad)) return LA_ERR_MISALIGNED;
@@ -239,6 +307,7 @@ la_status prefix_impl(const void *q, const void *k, const void *v, const void *k
     a.part_s = pa.part_s;
     a.part_z = pa.part_z;
     a.nseg = pa.nseg;
+    if (dtype == LA_DTYPE_BF16 && workspace_bytes >= L.total) plan_split(a, dev, ws + L.xfer);
     return to_status(run_prefill(a, dtype, cs));
 }
 
@@ -254,6 +323,33 @@ la_status la_prefill(const void *q, const void *k, const void *v, const float *s
                         eps, stream);
 }
 
+size_t la_prefill_workspace_size(int64_t B, int64_t H, int64_t N, int d_feat, la_dtype dtype) {
+    if (B < 1 || H < 1 || N < 0 || B > kMaxBH / H) return 0;
+    if (d_feat != kDFeat || dtype != LA_DTYPE_BF16) return 0;
+    return xfer_bytes(B * H) + xflag_bytes(B * H);
+}
+
+la_status la_prefill_split_info(int64_t B, int64_t H, int64_t N, int *split_heads, int *split_chunk) {
+    if (!split_heads || !split_chunk) return LA_ERR_INVALID_ARG;
+    *split_heads = *split_chunk = 0;
+    if (B < 1 || H < 1 || N < 0 || B > kMaxBH / H) return LA_ERR_INVALID_ARG;
+    int dev;
+    unsigned *status;
+    const la_status st = device_setup(&dev, &status);
+    if (st != LA_OK) return st;
+    const SplitPlan p = split_plan(B * H, N, g_sms[dev]);
+    *split_heads = p.r;
+    *split_chunk = p.n1;
+    return LA_OK;
+}
+
+la_status la_prefill_ws(const void *q, const void *k, const void *v, const float *s0, const float *z0, void *y,
+                        float *s_out, float *z_out, void *workspace, size_t workspace_bytes, int64_t B, int64_t H,
+                        int64_t N, int d_feat, int d_v, la_dtype dtype, float eps, la_stream_t stream) {
+    return prefill_impl(q, k, v, s0, z0, nullptr, y, s_out, z_out, B, H, N, d_feat, d_v, dtype, eps, stream,
+                        nullptr, false, workspace, workspace ? workspace_bytes : 0);
+}
+
 la_status la_prefill_padded(const void *q, const void *k, const void *v, const float *s0,
                             const float *z0, const int32_t *left_pad, void *y, float *s_out,
                             float *z_out, int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
@@ -267,6 +363,17 @@ size_t la_prefix_workspace_size(int64_t B, int64_t H, int64_t M) {
     if (B < 1 || H < 1 || M <= 0 || B > kMaxBH / H) return 0;
     return prefix_layout(B * H, M).total;
 }
+
+}  // extern "C"
+
+namespace la {
+size_t prefix_workspace_min(int64_t B, int64_t H, int64_t M) {
+    if (B < 1 || H < 1 || M <= 0 || B > kMaxBH / H) return 0;
+    return prefix_layout(B * H, M).base_total;
+}
+}  // namespace la
+
+extern "C" {
 
 la_status la_prefix_prefill(const void *q, const void *k, const void *v, const void *k_e,
                             const void *v_e, int64_t M, const float *s0, const float *z0,

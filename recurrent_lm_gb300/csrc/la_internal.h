@@ -50,6 +50,14 @@ struct PrefillArgs {
     // path the 273-row ones, part_s [BH][nseg][273][64] and part_z [BH][nseg][273].
     const float *part_s = nullptr, *part_z = nullptr;
     int64_t nseg = 0;
+    // Split heads (bf16 tensor-core path): the last split_r heads run as two
+    // pieces, chunks [0, split_n1) and [split_n1, n); the first hands its state
+    // to the second through xfer ([split_r][kXferFloats] fp32) and the flag
+    // words xflag ([split_r], set to call_id).  split_r = 0: no split.
+    int split_r = 0, split_n1 = 0;
+    float *xfer = nullptr;
+    unsigned long long *xflag = nullptr;
+    unsigned long long call_id = 0;
 };
 
 struct DecodeArgs {
@@ -74,6 +82,15 @@ struct PrefixArgs {
     const int32_t *left_pad;  // [B]: prefix positions j < min(left_pad[b], M) are padding
     int64_t N;                // causal length (the range of left_pad)
 };
+
+// Smallest workspace la_prefix_prefill accepts (the prefix partial states
+// only; la_prefix_workspace_size adds the split heads' hand-over region).
+size_t prefix_workspace_min(int64_t B, int64_t H, int64_t M);
+
+// One transfer slot of a split head: a state in the layout of s0 / s_out
+// ([273][64] values, then [273] z, fp32; or the 153-row compact layout),
+// padded to a multiple of 16 bytes.
+constexpr int kXferFloats = (kD * kDV + kD + 3) / 4 * 4;
 
 // Split of the M prefix tokens into segments, one CTA each: enough segments
 // for about 256 CTAs over all (b, h) (at most 16 per head, at least one

@@ -56,7 +56,9 @@ la_status la_prefix_prefill_noalloc(const void *q, const void *k, const void *v,
                                     void *y, float *s_out, float *z_out, int64_t B, int64_t H,
                                     int64_t N, int d_feat, int d_v, la_dtype dtype, float eps,
                                     la_stream_t stream) {
-    const size_t need = la_prefix_workspace_size(B, H, M);
+    // the full workspace when it fits, else the prefix partial states alone
+    // (the prefill then runs without split heads)
+    const size_t need = la::prefix_workspace_min(B, H, M);
     if (need > kScratchBytes) return LA_ERR_SCRATCH_TOO_SMALL;
     void *scratch = nullptr;
     if (need > 0) {

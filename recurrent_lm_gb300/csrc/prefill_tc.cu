@@ -245,6 +245,39 @@ __device__ __forceinline__ void add_partials(const float *part, int64_t stride, 
     }
 }
 
+// A head split in two pieces hands its state over through a transfer slot
+// (kXferFloats floats): the first piece writes its final state there as it
+// would to s_out (same layout: values, then z) and then publishes a flag word
+// equal to the launch's call id; the second piece waits for it (bounded) and
+// reads the slot as its initial state.
+static_assert(kXferFloats >= kD * kDV + kD && kXferFloats % 4 == 0, "transfer slot");
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Bounded wait for *flag == v (about one second); on expiry the timeout is
+// recorded and the CTA's abort flag set.
+__device__ __forceinline__ bool wait_flag(const unsigned long long *flag, unsigned long long v,
+                                          volatile int *abort, unsigned *status) {
+    const long long t0 = clock64();
+    while (ld_acquire_u64(flag) != v) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            atomicOr(status, kStatusTimeout);
+            *abort = 1;
+            return false;
+        }
+        __nanosleep(256);
+    }
+    return true;
+}
+
 // Image of one head's final [273][64] fp32 state in shared memory, written
 // out with a single bulk copy once the last update has completed (the
 // feature-operand buffers it overlays are free by then).
@@ -284,7 +317,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                   const float *__restrict__ gamma, int64_t H,
                   float *__restrict__ s_out, float *__restrict__ z_out, int N, float eps,
                   unsigned *status, const float *__restrict__ part_s, const float *__restrict__ part_z,
-                  int nseg) {
+                  int nseg, int bh_total, int split_r, int split_n1, float *__restrict__ xfer,
+                  unsigned long long *__restrict__ xflag, unsigned long long call_id) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -293,20 +327,49 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     volatile int *abort = reinterpret_cast<volatile int *>(smem + kSmAbort);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t bh = blockIdx.x;
 #ifdef LA_TRACE
     const long long t_start = clock64();
 #endif
-    const int n = (N + kC - 1) / kC;
+    // Work of this CTA: a whole head, or a piece of one of the last split_r
+    // heads, which are split at chunk split_n1.  Block order: split_r whole
+    // heads, the split_r first pieces, the other whole heads, the split_r
+    // second pieces (launch_prefill_tc explains the schedule).
+    const int n_all = (N + kC - 1) / kC;
+    int64_t bh_ = blockIdx.x;
+    int c0_ = 0, n_ = n_all, piece_ = 0;  // piece 0: whole head, 1: first piece, 2: second piece
+    if (split_r > 0) {
+        const int b = blockIdx.x;
+        if (b < split_r) {
+        } else if (b < 2 * split_r) {
+            bh_ = bh_total - split_r + (b - split_r);
+            n_ = split_n1;
+            piece_ = 1;
+        } else if (b < bh_total) {
+            bh_ = b - split_r;
+        } else {
+            bh_ = bh_total - split_r + (b - bh_total);
+            c0_ = split_n1;
+            n_ = n_all - split_n1;
+            piece_ = 2;
+        }
+    }
+    const int64_t bh = bh_;
+    const int c0 = c0_;   // first chunk of this CTA's work
+    const int n = n_;     // chunks of this CTA's work
+    const int piece = piece_;
+    float *xs = piece ? xfer + (bh - (bh_total - split_r)) * (int64_t)kXferFloats : nullptr;
+    unsigned long long *xf = piece ? xflag + (bh - (bh_total - split_r)) : nullptr;
     // leading padding positions of this batch row: no contribution to any sum, y = 0
     const int lpad = kPad ? (int)row_left_pad(left_pad, bh / H, N, status, tid == 0) : 0;
     // per-head columns of the state in memory (the 273-row layout, or with
     // kCompact the 153-row one): entry (row r, value d) at [r * 64 + d]
     constexpr int64_t kRowsIO = kCompact ? kDCompact : kD;
-    const float *s0h = s0 ? s0 + bh * kRowsIO * kDV : nullptr;
-    const float *z0h = z0 ? z0 + bh * kRowsIO : nullptr;
-    float *s_outh = s_out ? s_out + bh * kRowsIO * kDV : nullptr;
-    float *z_outh = z_out ? z_out + bh * kRowsIO : nullptr;
+    // a second piece starts from the transfer slot (which holds s0 and, for
+    // the prefix call, the prefix sum already); a first piece ends there
+    const float *s0h = piece == 2 ? xs : (s0 ? s0 + bh * kRowsIO * kDV : nullptr);
+    const float *z0h = piece == 2 ? xs + kRowsIO * kDV : (z0 ? z0 + bh * kRowsIO : nullptr);
+    float *s_outh = piece == 1 ? xs : (s_out ? s_out + bh * kRowsIO * kDV : nullptr);
+    float *z_outh = piece == 1 ? xs + kRowsIO * kDV : (z_out ? z_out + bh * kRowsIO : nullptr);
 
     // ---- set-up: barriers, TMEM, constant operands, feature -> row table
     if (tid == 0) {
@@ -361,7 +424,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         __syncthreads();
     }
     // length of chunk c (the last may be short)
-    auto chunk_len = [&](int c) { return min(kC, N - c * kC); };
+    auto chunk_len = [&](int c) { return min(kC, N - (c0 + c) * kC); };
     // the antisymmetric part of s0 bypasses the compact state: it decays by gamma^N
     const float anti_decay = kDecay ? powf(pow_gamma(1), (float)N) : 1.f;
 
@@ -375,10 +438,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         prefetch_tmap(&tv);
         for (int c = 0; c < n_early; ++c) {
             mbar_expect_tx(bar(B_QK_FULL + c), 2 * kC * 16 * 2);
-            tma_load_3d(sb + kSmQ + c * 4096, &tq, bar(B_QK_FULL + c), 0, c * kC, (int)bh);
-            tma_load_3d(sb + kSmK + c * 4096, &tk, bar(B_QK_FULL + c), 0, c * kC, (int)bh);
+            tma_load_3d(sb + kSmQ + c * 4096, &tq, bar(B_QK_FULL + c), 0, (c0 + c) * kC, (int)bh);
+            tma_load_3d(sb + kSmK + c * 4096, &tk, bar(B_QK_FULL + c), 0, (c0 + c) * kC, (int)bh);
             mbar_expect_tx(bar(B_V_FULL + c), kC * 64 * 2);
-            tma_load_3d(sb + kSmV + c * 16384, &tv, bar(B_V_FULL + c), 0, c * kC, (int)bh);
+            tma_load_3d(sb + kSmV + c * 16384, &tv, bar(B_V_FULL + c), 0, (c0 + c) * kC, (int)bh);
         }
     }
 
@@ -393,6 +456,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
         const float *col0 = zrow ? z0h : (s0h ? s0h + d : nullptr);
         const int64_t stride = zrow ? 1 : kDV;
+        // a second piece waits until its first piece has handed its state over
+        if (piece == 2) __all_sync(0xffffffffu, wait_flag(xf, call_id, abort, status));
         auto load_group = [&](auto gc) {
             constexpr int G = decltype(gc)::value;
             uint32_t r[32];
@@ -401,9 +466,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             else
                 compact_initial_group<G>(col0, stride, r, std::make_integer_sequence<int, 32>{});
             if constexpr (kPrefix) {
-                // + the prefix segments' partial states (internal compact rows), in order
+                // + the prefix segments' partial states (internal compact rows), in
+                // order; a second piece's slot holds them already
                 const float *p = zrow ? part_z + bh * nseg * kNFeat : part_s + bh * nseg * kNFeat * kDV + d;
-                add_partials<G>(p, stride, zrow ? kNFeat : kNFeat * kDV, nseg, r);
+                add_partials<G>(p, stride, zrow ? kNFeat : kNFeat * kDV, piece == 2 ? 0 : nseg, r);
             }
             __syncwarp();
             if (!zrow || lane == 0) write_sb_group(sb + kSmSb, zrow ? 64 : d, G, r);
@@ -444,15 +510,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 if (!mbar_wait(bar(B_QK_EMPTY + st), ph, abort, status)) break;
                 LA_TR(TR_TMA, c, 0);
                 mbar_expect_tx(bar(B_QK_FULL + st), 2 * kC * 16 * 2);
-                tma_load_3d(sb + kSmQ + st * 4096, &tq, bar(B_QK_FULL + st), 0, c * kC, (int)bh);
-                tma_load_3d(sb + kSmK + st * 4096, &tk, bar(B_QK_FULL + st), 0, c * kC, (int)bh);
+                tma_load_3d(sb + kSmQ + st * 4096, &tq, bar(B_QK_FULL + st), 0, (c0 + c) * kC, (int)bh);
+                tma_load_3d(sb + kSmK + st * 4096, &tk, bar(B_QK_FULL + st), 0, (c0 + c) * kC, (int)bh);
                 issued_qk = c + 1;
                 if (!mbar_wait(bar(B_V_EMPTY + st), ph, abort, status)) break;
                 LA_TR(TR_TMA, c, 1);
                 mbar_expect_tx(bar(B_V_FULL + st), kC * 64 * 2);
-                tma_load_3d(sb + kSmV + st * 16384, &tv, bar(B_V_FULL + st), 0, c * kC, (int)bh);
+                tma_load_3d(sb + kSmV + st * 16384, &tv, bar(B_V_FULL + st), 0, (c0 + c) * kC, (int)bh);
                 issued_v = c + 1;
-                if (!kCompact && c == n - 1 && s0h) {
+                if (!kCompact && c == n - 1 && s0h && piece != 1) {
                     // the final state store reads s0 again (its antisymmetric part)
                     prefetch_l2_bulk(s0h, (uint32_t)kD * kDV * 4);
                     for (int o = 0; o < kD; o += 32) prefetch_l2(z0h + o);
@@ -556,7 +622,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (!__all_sync(0xffffffffu, mbar_wait(bar(B_T_FULL), (uint32_t)c & 1u, abort, status))) break;
             tc_fence_after();
             // P V of chunk c - 1 completed with the read-out (NUM_FULL(c - 1))
-            if (!p_block<kPad, kDecay>(tmem + lanebase + kTmT, tmem + lanebase + kTmP + 32, 1, i, w, kmin - c * kC,
+            if (!p_block<kPad, kDecay>(tmem + lanebase + kTmT, tmem + lanebase + kTmP + 32, 1, i, w,
+                                       kmin - (c0 + c) * kC,
                                        sb + kSmPow, c > 0 ? bar(B_NUM_FULL) : 0u, (uint32_t)(c - 1) & 1u, abort,
                                        status))
                 break;
@@ -599,8 +666,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (lane == 0) mbar_arrive(bar(B_RO_READY));
             if (tid == 128) LA_TR(TR_GEN, c, 1);
             // past the end or left padding: no contribution to S', z'
-            bool pad = c * kC + t >= N;
-            if constexpr (kPad) pad = pad || c * kC + t < lpad;
+            bool pad = (c0 + c) * kC + t >= N;
+            if constexpr (kPad) pad = pad || (c0 + c) * kC + t < lpad;
             // the update of chunk c - 1 (S_FULL) released the Phi'_K buffer and V(c - 1)
             if (!mbar_wait(bar(B_S_FULL), pc ^ 1u, abort, status)) break;
             if (c > 0 && tid == 128) LA_TR(TR_CONV, c - 1, 2);
@@ -646,13 +713,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                                           s_outh, z0h, z_outh, anti_decay, std::make_integer_sequence<int, 2>{});
             }
             fence_async_smem();
+            if (piece == 1) __threadfence();  // the z' row, before the hand-over flag
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_STAGED));
-            // every value row is in the image: one bulk copy to s_out
+            // every value row is in the image: one bulk copy to s_out (a first
+            // piece: to its transfer slot, then the hand-over flag)
             if (tid == 128 && s_outh && mbar_wait(bar(B_STAGED), 0u, abort, status)) {
                 bulk_store(s_outh, sb + kSmStage, kCompact ? kStageBytesCompact : kStageBytes);
                 bulk_commit();
                 bulk_wait0();
+                if (piece == 1) {
+                    __threadfence();
+                    st_release_u64(xf, call_id);
+                }
             }
             if (tid == 128) LA_TR(TR_CONV, n - 1, 5);
         }
@@ -674,7 +747,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (tid == 256) mbar_arrive(bar(B_QK_EMPTY + c % kStages));  // Q K^T(c) has read its q, k stage
             if (tid == 256 + 96) LA_TR(TR_EPI, c, 0);
             tc_fence_after();
-            const int kmin = kPad ? lpad - c * kC : 0;  // keys below kmin are left padding
+            const int kmin = kPad ? lpad - (c0 + c) * kC : 0;  // keys below kmin are left padding
             // keys 0..63 -> P columns 0..31; keys 64..127 of lane quarters 2, 3 are
             // warps 2, 3's share (P columns 32..63).  The store waits until P V of
             // chunk c - 1 has completed (NUM_FULL(c - 1)).
@@ -716,6 +789,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             if (last) {
                 fence_async_smem();
+                if (piece == 1) __threadfence();  // the z' row, before the hand-over flag
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_STAGED));
             } else {
@@ -761,7 +835,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 // (rows past N are clipped by the store)
                 float inv = 1.0f / (__uint_as_float(dr) + eps);
                 if constexpr (kPad)
-                    if (c * kC + i < lpad) inv = 0.f;  // padded query rows (left padding) output 0
+                    if ((c0 + c) * kC + i < lpad) inv = 0.f;  // padded query rows (left padding) output 0
                 const uint64_t inv2 = f2pack(inv, inv);
                 const uint32_t stage = sb + kSmY + (uint32_t)w * 4096;
                 if (lane == 0) bulk_wait_read0();  // previous chunk's store has read the tile
@@ -777,8 +851,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 }
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0 && c * kC + 32 * w < N) {
-                    tma_store_3d(&ty, stage, 0, c * kC + 32 * w, (int)bh);
+                if (lane == 0 && (c0 + c) * kC + 32 * w < N) {
+                    tma_store_3d(&ty, stage, 0, (c0 + c) * kC + 32 * w, (int)bh);
                     bulk_commit();
                 }
             }
@@ -879,30 +953,28 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     const bool prefix = a.part_s != nullptr;
     if (prefix && (a.gamma || a.compact || a.nseg < 1 || a.nseg > 65535)) return cudaErrorInvalidValue;
     const int nseg = (int)a.nseg;
+    // split heads (see the schedule above): grid = BH + split_r
+    const int r = a.split_r;
+    if (r < 0 || (r > 0 && (!a.xfer || !a.xflag || 2 * (int64_t)r > BH || a.split_n1 < 1 ||
+                            a.split_n1 >= (a.N + kC - 1) / kC)))
+        return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)(BH + r);
+#define LA_PREFILL_ARGS                                                                                    \
+    tq, tk, tv, ty, a.s0, a.z0, a.left_pad, a.gamma, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status, a.part_s, \
+        a.part_z, nseg, (int)BH, r, a.split_n1, a.xfer, a.xflag, a.call_id
     if (prefix && a.left_pad)
-        prefill_tc_kernel<true, false, false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, a.left_pad, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
-            a.part_s, a.part_z, nseg);
+        prefill_tc_kernel<true, false, false, true><<<grid, kThreads, kSmAlloc, st>>>(LA_PREFILL_ARGS);
     else if (prefix)
-        prefill_tc_kernel<false, false, false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
-            a.part_s, a.part_z, nseg);
+        prefill_tc_kernel<false, false, false, true><<<grid, kThreads, kSmAlloc, st>>>(LA_PREFILL_ARGS);
     else if (a.compact)
-        prefill_tc_kernel<false, false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
-            nullptr, nullptr, 0);
+        prefill_tc_kernel<false, false, true><<<grid, kThreads, kSmAlloc, st>>>(LA_PREFILL_ARGS);
     else if (a.left_pad)
-        prefill_tc_kernel<true, false><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, a.left_pad, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
-            nullptr, nullptr, 0);
+        prefill_tc_kernel<true, false><<<grid, kThreads, kSmAlloc, st>>>(LA_PREFILL_ARGS);
     else if (a.gamma)
-        prefill_tc_kernel<false, true><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, nullptr, a.gamma, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
-            nullptr, nullptr, 0);
+        prefill_tc_kernel<false, true><<<grid, kThreads, kSmAlloc, st>>>(LA_PREFILL_ARGS);
     else
-        prefill_tc_kernel<false, false><<<(unsigned)BH, kThreads, kSmAlloc, st>>>(
-            tq, tk, tv, ty, a.s0, a.z0, nullptr, nullptr, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status,
-            nullptr, nullptr, 0);
+        prefill_tc_kernel<false, false><<<grid, kThreads, kSmAlloc, st>>>(LA_PREFILL_ARGS);
+#undef LA_PREFILL_ARGS
     return cudaGetLastError();
 }
 

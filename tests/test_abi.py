@@ -118,9 +118,12 @@ def test_prefix_rejects_small_or_misaligned_workspace(lib):
     assert need > 0 and need % 256 == 0
     assert lib.la_prefix_workspace_size(2, 3, 0) == 0
     p = [fake(i) for i in range(12)]
+    # smaller than the prefix partial states (at least 3 segments x 6 heads x 70,980 B):
+    # rejected; between that and `need` the call runs without split heads
     rc = lib.la_prefix_prefill(p[0], p[1], p[2], p[3], p[4], 5000, p[5], p[6], p[7], p[8], p[9],
-                               p[10], need - 1, 2, 3, 8000, 16, 64, 1, 0.0, None)
+                               p[10], 6 * 3 * 70980 - 1, 2, 3, 8000, 16, 64, 1, 0.0, None)
     assert rc == binding.LA_ERR_INVALID_ARG
+    assert need > 6 * 3 * 70980
     ws = ctypes.c_void_p(p[10].value + 16)   # 16- but not 256-byte aligned
     rc = lib.la_prefix_prefill(p[0], p[1], p[2], p[3], p[4], 5000, p[5], p[6], p[7], p[8], p[9],
                                ws, need, 2, 3, 8000, 16, 64, 1, 0.0, None)
