@@ -96,8 +96,10 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // So r SMs run whole heads and then a second piece, and the other SMs run
 // k = ceil(r / (SMs - r)) first pieces before their whole heads; the first
 // pieces are done long before the second pieces start (blocks are dispatched
-// in order).  n1 balances the two kinds of SM, counting f = 10 chunk times of
-// fixed cost per CTA (set-up and final state): n - n1 + f = k (n1 + f).
+// in order).  n1 balances the two kinds of SM, counting f chunk times of fixed
+// cost per CTA (set-up and final state): n - n1 + f = k (n1 + f).  f = 16 was
+// measured best (f = 6 / 10 / 14 / 18 / 24 at B=16, H=16, N=32768: 0.607 /
+// 0.599 / 0.591 / 0.588 / 0.592 ms; the prefix call is best at 14).
 struct SplitPlan {
     int r = 0, n1 = 0;
 };
@@ -110,7 +112,7 @@ SplitPlan split_plan(int64_t BH, int64_t N, int sms) {
     const int64_t r = BH - (W - 1) * sms;
     if (r <= 0 || r >= sms) return p;
     const int64_t k = (r + (sms - r) - 1) / (sms - r);
-    const int64_t f = 10;
+    const int64_t f = 16;
     const int64_t n2 = (k * n + (k - 1) * f) / (k + 1);
     const int64_t n1 = n - n2;
     if (n1 < 4 || n2 < 4) return p;
