@@ -43,6 +43,21 @@ def test_decayed_prefill(dtype, N):
     check(got, ref, TOL[dtype], f" N={N}")
 
 
+@pytest.mark.parametrize("N", [2999, 4100])
+def test_decayed_prefill_across_epochs(N):
+    """bf16 decayed prefill over 24 to 33 chunks with rates from 1 down to 0.3
+    (for 0.3 the state before a chunk is below 2^-200 of its value after 128
+    tokens), ragged N: y and the final state against the oracle."""
+    g = [1.0, 0.999, 0.9375, 0.8, 0.6, 0.55, 0.3, 0.99]
+    q, k, v, _, _ = inputs.qkv(1, len(g), N, seed=1150 + N, dtype=torch.bfloat16)
+    s0, z0 = inputs.random_state(1, len(g), seed=1151)
+    g32 = torch.tensor(g, dtype=torch.float32)
+    got = la.prefill(q.to(DEV), k.to(DEV), v.to(DEV), s0.to(DEV), z0.to(DEV), gamma=g32.to(DEV))
+    la.check_device_status()
+    ref = oracle.prefill_decay(q, k, v, g32.double().numpy(), s0, z0)
+    check(got, ref, TOL[torch.bfloat16], f" N={N}")
+
+
 def test_decay_of_one_is_the_plain_prefill():
     q, k, v, _, _ = inputs.qkv(2, 3, 700, seed=1110)
     s0, z0 = inputs.random_state(2, 3, seed=1111)
