@@ -402,12 +402,13 @@ def leg_prefill_decay(la, args, dist, dev):
 
 
 def leg_general_dk(la, args, dist, dev):
-    """la_prefill on the general feature-dimension path (d' = 8, 24, 32) at
-    B=4, H=16, N=4096, bf16, with an initial state."""
+    """la_prefill at other feature dimensions, bf16, with an initial state:
+    d' = 8 on the tensor cores (the padded map) at the long-prefill shape B=16,
+    H=16, N=32768; d' = 24, 32 on the CUDA-core path at B=4, H=16, N=4096."""
     out = {}
     for dk in (8, 24, 32):
         D = 1 + dk + dk * dk
-        B, H, N = 4, 16, 4096
+        B, H, N = (16, 16, 32768) if dk == 8 else (4, 16, 4096)
         g = torch.Generator(device=dev)
         g.manual_seed(shard_seed(1500 + dk, dist.rank))
         q = gen_device((B, H, N, dk), g, dev=dev)
@@ -422,9 +423,10 @@ def leg_general_dk(la, args, dist, dev):
         def step():
             la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z)
 
-        ms = time_loop(step, max(1, args.steps // 20), 3, dist)
+        ms = time_loop(step, max(1, args.steps // (4 if dk == 8 else 20)), 3, dist)
         la.check_device_status()
-        out[dk] = {"ms": ms, "B": B, "H": H, "N": N, "D": D}
+        out[dk] = {"ms": ms, "B": B, "H": H, "N": N, "D": D,
+                   "path": "tensor cores (padded d' = 16 map)" if dk == 8 else "CUDA cores (general d')"}
     return out
 
 
@@ -701,8 +703,9 @@ def main():
             line["legs"][f"prefill_dk{dk}"] = {
                 "workload": f"prefill-bf16-B{r['B']}-H{r['H']}-N{r['N']}-dk{dk}-D{r['D']}-s0",
                 "ms_per_call": r["ms"], "tokens_per_s": W * r["B"] * r["N"] / t,
-                "achieved_tflops": fl / t / 1e12, "path": "CUDA cores (general d')"}
-            launches += max(1, args.steps // 20)
+                "achieved_tflops": fl / t / 1e12, "tc_frac": fl / t / 1e12 / pk["bf16_tflops"],
+                "path": r["path"]}
+            launches += max(1, args.steps // (4 if dk == 8 else 20))
     suffix = {"decode": "", "decode_decay": "-decay-1-2^-(4+h)", "decode_compact": "-compact-state-153"}
     for dname in ("decode", "decode_decay", "decode_compact"):
         if dname not in res:

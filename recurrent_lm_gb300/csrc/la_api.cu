@@ -165,8 +165,12 @@ cudaError_t run_prefill(const la::PrefillArgs &a, la_dtype dtype, cudaStream_t s
         return la::launch_state_copy(a.compact ? la::kDCompact : la::feat_dim(dk), a.s0, a.z0, a.s_out,
                                      a.z_out, BH, st);
     }
+    if (dtype == LA_DTYPE_BF16 && (dk == kDFeat || dk == 8)) {  // tensor cores (d' = 8: padded map)
+        la::PrefillArgs b = a;
+        b.dk = dk;
+        return la::launch_prefill_tc(b, st);
+    }
     if (dk != kDFeat) return la::launch_prefill_general(a, dk, dtype, st);
-    if (dtype == LA_DTYPE_BF16) return la::launch_prefill_tc(a, st);
     return la::launch_prefill_simt(a, dtype, st);
 }
 
@@ -243,7 +247,7 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
     la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad, gamma};
     a.compact = compact;
     // split heads on the bf16 tensor-core path, given room for the hand-over
-    if (workspace && dtype == LA_DTYPE_BF16 && d_feat == kDFeat && !gamma &&
+    if (workspace && dtype == LA_DTYPE_BF16 && (d_feat == kDFeat || d_feat == 8) && !gamma &&
         workspace_bytes >= xfer_bytes(BH) + xflag_bytes(BH))
         plan_split(a, dev, static_cast<char *>(workspace));
     return to_status(run_prefill(a, dtype, reinterpret_cast<cudaStream_t>(stream), d_feat));
@@ -327,7 +331,7 @@ la_status la_prefill(const void *q, const void *k, const void *v, const float *s
 
 size_t la_prefill_workspace_size(int64_t B, int64_t H, int64_t N, int d_feat, la_dtype dtype) {
     if (B < 1 || H < 1 || N < 0 || B > kMaxBH / H) return 0;
-    if (d_feat != kDFeat || dtype != LA_DTYPE_BF16) return 0;
+    if ((d_feat != kDFeat && d_feat != 8) || dtype != LA_DTYPE_BF16) return 0;
     return xfer_bytes(B * H) + xflag_bytes(B * H);
 }
 

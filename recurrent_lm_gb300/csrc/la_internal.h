@@ -44,6 +44,7 @@ struct PrefillArgs {
     const int32_t *left_pad;  // [B] leading padding positions per batch row, or NULL
     const float *gamma;       // [H] per-head decay in [0, 1], or NULL (no decay)
     bool compact = false;     // s0/z0 and s_out/z_out in the 153-row compact layout
+    int dk = 16;              // d' (the tensor-core path: 16, or 8 on the padded map)
     // Prefix partial states added, segment by segment in order, to the initial
     // state (NULL: none): the bf16 tensor-core path reads its internal compact
     // rows, part_s [BH][nseg][160][64] and part_z [BH][nseg][160]; the fp32

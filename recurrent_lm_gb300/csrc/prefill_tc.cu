@@ -171,13 +171,15 @@ __device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, i
 // wait gave up.  Kept out of line: the six P warps share one copy of this
 // code (the kernel's roles together run more code than the instruction cache
 // holds).
-template <bool kPad, bool kDecay>
+template <bool kPad, bool kDecay, int kDk = 16>
 static __device__ __noinline__ bool p_block(uint32_t tsrc, uint32_t tdst, int pp, int i, int w, int kmin,
                                             uint32_t pow, uint32_t wbar, uint32_t wpar, volatile int *abort,
                                             unsigned *status) {
     uint32_t pw[32];
     {
-        const uint64_t c32 = f2pack(0.03125f, 0.03125f), c4 = f2pack(0.25f, 0.25f), c1 = f2pack(1.0f, 1.0f);
+        // K(q, k) = 1 + q.k / sqrt(d') + (q.k)^2 / (2 d')
+        constexpr float kLin = kDk == 16 ? 0.25f : 0.35355339059327376f, kQuad = 1.0f / (2 * kDk);
+        const uint64_t c32 = f2pack(kQuad, kQuad), c4 = f2pack(kLin, kLin), c1 = f2pack(1.0f, 1.0f);
         const bool diag = 64 * pp + 63 >= 32 * w;  // this block reaches the diagonal
         if constexpr (kDecay) {
             // times the decay factors (gamma^(i-j), gamma^(i-j-1)) from the power
@@ -308,7 +310,7 @@ enum { TR_TMA = 0, TR_MMA, TR_GEN, TR_EPI, TR_CONV };
 // writes gamma^(L-1-t) Phi'_K (scaled key features), the intra-chunk kernel
 // entries carry gamma^(i-j), and the state is multiplied by gamma^L in TMEM
 // before each update.
-template <bool kPad, bool kDecay, bool kCompact = false, bool kPrefix = false>
+template <bool kPad, bool kDecay, bool kCompact = false, bool kPrefix = false, int kDk = 16>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty,
@@ -363,7 +365,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int lpad = kPad ? (int)row_left_pad(left_pad, bh / H, N, status, tid == 0) : 0;
     // per-head columns of the state in memory (the 273-row layout, or with
     // kCompact the 153-row one): entry (row r, value d) at [r * 64 + d]
-    constexpr int64_t kRowsIO = kCompact ? kDCompact : kD;
+    constexpr int64_t kRowsIO = kCompact ? kDCompact : (kDk == 8 ? 73 : kD);
     // a second piece starts from the transfer slot (which holds s0 and, for
     // the prefix call, the prefix sum already); a first piece ends there
     const float *s0h = piece == 2 ? xs : (s0 ? s0 + bh * kRowsIO * kDV : nullptr);
@@ -464,7 +466,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if constexpr (kCompact)
                 compact_io_initial_group<G>(col0, stride, r, std::make_integer_sequence<int, 32>{});
             else
-                compact_initial_group<G>(col0, stride, r, std::make_integer_sequence<int, 32>{});
+                compact_initial_group<G, kDk>(col0, stride, r, std::make_integer_sequence<int, 32>{});
             if constexpr (kPrefix) {
                 // + the prefix segments' partial states (internal compact rows), in
                 // order; a second piece's slot holds them already
@@ -520,8 +522,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 issued_v = c + 1;
                 if (!kCompact && c == n - 1 && s0h && piece != 1) {
                     // the final state store reads s0 again (its antisymmetric part)
-                    prefetch_l2_bulk(s0h, (uint32_t)kD * kDV * 4);
-                    for (int o = 0; o < kD; o += 32) prefetch_l2(z0h + o);
+                    prefetch_l2_bulk(s0h, (uint32_t)kRowsIO * kDV * 4);
+                    for (int o = 0; o < kRowsIO; o += 32) prefetch_l2(z0h + o);
                 }
             }
             if (*abort) {
@@ -622,7 +624,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (!__all_sync(0xffffffffu, mbar_wait(bar(B_T_FULL), (uint32_t)c & 1u, abort, status))) break;
             tc_fence_after();
             // P V of chunk c - 1 completed with the read-out (NUM_FULL(c - 1))
-            if (!p_block<kPad, kDecay>(tmem + lanebase + kTmT, tmem + lanebase + kTmP + 32, 1, i, w,
+            if (!p_block<kPad, kDecay, kDk>(tmem + lanebase + kTmT, tmem + lanebase + kTmP + 32, 1, i, w,
                                        kmin - (c0 + c) * kC,
                                        sb + kSmPow, c > 0 ? bar(B_NUM_FULL) : 0u, (uint32_t)(c - 1) & 1u, abort,
                                        status))
@@ -656,10 +658,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tc_fence_after();
             if constexpr (kDecay) {  // token t reads gamma^(t+1) of the state before the chunk
                 const float lq = pow_gamma(t + 1);
-                emit_features_tmem<false, true>(qlo, qhi, tmem + lanebase + kTmPhiQ,
+                emit_features_tmem<false, true, kDk>(qlo, qhi, tmem + lanebase + kTmPhiQ,
                                                 std::make_integer_sequence<int, 5>{}, pack_bf16(lq, lq));
             } else {
-                emit_features_tmem<false>(qlo, qhi, tmem + lanebase + kTmPhiQ, std::make_integer_sequence<int, 5>{});
+                emit_features_tmem<false, false, kDk>(qlo, qhi, tmem + lanebase + kTmPhiQ,
+                                                      std::make_integer_sequence<int, 5>{});
             }
             tc_fence_before();
             __syncwarp();
@@ -687,10 +690,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (tid == 128) LA_TR(TR_GEN, c, 2);
             if constexpr (kDecay) {  // token t enters the state after the chunk with gamma^(L-1-t)
                 const float lk = pow_gamma(max(chunk_len(c) - 1 - t, 0));
-                emit_features<true, true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{},
+                emit_features<true, true, kDk>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{},
                                           pack_bf16(lk, lk));
             } else {
-                emit_features<true>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
+                emit_features<true, false, kDk>(klo, khi, sb + kSmPhiK, t, pad, std::make_integer_sequence<int, 20>{});
             }
             fence_async_smem();
             __syncwarp();
@@ -709,7 +712,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     final_groups_compact<true, 3>(tmem + lanebase + kTmS, 32 * wq + lane, zrow, lane,
                                                   sb + kSmStage, s_outh, z_outh, std::make_integer_sequence<int, 2>{});
                 else
-                    final_groups<true, 3>(tmem + lanebase + kTmS, 32 * wq + lane, zrow, lane, s0h, sb + kSmStage,
+                    final_groups<true, 3, kDk>(tmem + lanebase + kTmS, 32 * wq + lane, zrow, lane, s0h, sb + kSmStage,
                                           s_outh, z0h, z_outh, anti_decay, std::make_integer_sequence<int, 2>{});
             }
             fence_async_smem();
@@ -719,7 +722,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // every value row is in the image: one bulk copy to s_out (a first
             // piece: to its transfer slot, then the hand-over flag)
             if (tid == 128 && s_outh && mbar_wait(bar(B_STAGED), 0u, abort, status)) {
-                bulk_store(s_outh, sb + kSmStage, kCompact ? kStageBytesCompact : kStageBytes);
+                bulk_store(s_outh, sb + kSmStage, kCompact ? kStageBytesCompact : (uint32_t)kRowsIO * kDV * 4);
                 bulk_commit();
                 bulk_wait0();
                 if (piece == 1) {
@@ -751,7 +754,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             // keys 0..63 -> P columns 0..31; keys 64..127 of lane quarters 2, 3 are
             // warps 2, 3's share (P columns 32..63).  The store waits until P V of
             // chunk c - 1 has completed (NUM_FULL(c - 1)).
-            if (!p_block<kPad, kDecay>(tmem + lanebase + kTmT, tmem + lanebase + kTmP, 0, i, w, kmin, sb + kSmPow,
+            if (!p_block<kPad, kDecay, kDk>(tmem + lanebase + kTmT, tmem + lanebase + kTmP, 0, i, w, kmin, sb + kSmPow,
                                        c > 0 ? bar(B_NUM_FULL) : 0u, (uint32_t)(c - 1) & 1u, abort, status))
                 return false;
             tc_fence_before();
@@ -782,7 +785,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     final_groups_compact<true, 0>(tmem + lanebase + kTmS, i, zrow, lane, sb + kSmStage, s_outh,
                                                   z_outh, std::make_integer_sequence<int, 3>{});
                 } else {
-                    final_groups<true, 0>(tmem + lanebase + kTmS, i, zrow, lane, s0h, sb + kSmStage, s_outh, z0h,
+                    final_groups<true, 0, kDk>(tmem + lanebase + kTmS, i, zrow, lane, s0h, sb + kSmStage, s_outh, z0h,
                                           z_outh, anti_decay, std::make_integer_sequence<int, 3>{});
                 }
                 __syncwarp();
@@ -904,12 +907,12 @@ EncodeFn encode_fn() {
 // [BH][N][width] bf16 rows as a 3-D tensor map with a {width, 128, 1} box;
 // rows past N read as zero.
 bool make_row_tmap(CUtensorMap *map, const void *base, int64_t BH, int64_t N, int width,
-                   bool swizzle128, int box_rows) {
+                   bool swizzle128, int box_rows, int box_width) {
     EncodeFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)N, (cuuint64_t)BH};
     const cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)N * width * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)width, (cuuint32_t)box_rows, 1u};
+    const cuuint32_t box[3] = {(cuuint32_t)(box_width ? box_width : width), (cuuint32_t)box_rows, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -921,7 +924,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
     const int64_t BH = a.B * a.H;
     if (a.N > (int64_t)0x7FFFFFFF - kC) return cudaErrorInvalidValue;
     CUtensorMap tq, tk, tv, ty;
-    if (!make_row_tmap(&tq, a.q, BH, a.N, 16, false) || !make_row_tmap(&tk, a.k, BH, a.N, 16, false) ||
+    // d' = 8: the q, k rows are 8 wide; the box reads 16 columns, the upper 8
+    // out of bounds and so zero (the padded rows of the d' = 16 map)
+    if (a.dk != 16 && a.dk != 8) return cudaErrorInvalidValue;
+    if (!make_row_tmap(&tq, a.q, BH, a.N, a.dk, false, 128, 16) ||
+        !make_row_tmap(&tk, a.k, BH, a.N, a.dk, false, 128, 16) ||
         !make_row_tmap(&tv, a.v, BH, a.N, 64, true) || !make_row_tmap(&ty, a.y, BH, a.N, 64, true, 32))
         return cudaErrorInvalidValue;
     static int configured_for = -1;
@@ -945,6 +952,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(prefill_tc_kernel<true, false, false, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<false, false, false, false, 8>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
@@ -962,7 +972,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t st) {
 #define LA_PREFILL_ARGS                                                                                    \
     tq, tk, tv, ty, a.s0, a.z0, a.left_pad, a.gamma, a.H, a.s_out, a.z_out, (int)a.N, a.eps, a.status, a.part_s, \
         a.part_z, nseg, (int)BH, r, a.split_n1, a.xfer, a.xflag, a.call_id
-    if (prefix && a.left_pad)
+    // d' = 8: the plain prefill only (padding, decay, the prefix and the compact
+    // state exist for d' = 16)
+    if (a.dk == 8 && (prefix || a.compact || a.left_pad || a.gamma)) return cudaErrorInvalidValue;
+    if (a.dk == 8)
+        prefill_tc_kernel<false, false, false, false, 8><<<grid, kThreads, kSmAlloc, st>>>(LA_PREFILL_ARGS);
+    else if (prefix && a.left_pad)
         prefill_tc_kernel<true, false, false, true><<<grid, kThreads, kSmAlloc, st>>>(LA_PREFILL_ARGS);
     else if (prefix)
         prefill_tc_kernel<false, false, false, true><<<grid, kThreads, kSmAlloc, st>>>(LA_PREFILL_ARGS);

@@ -115,17 +115,40 @@ __device__ __forceinline__ void emit_chunk(const uint32_t (&XL)[8], const uint32
     st_shared_v4(base + feat_chunk_off<kKey>(J, t), w0, w1, w2, w3);
 }
 
+// xbar as packed bf16 pairs from the raw token row.  kDk = 16: xbar = x / 2
+// (exact).  kDk = 8: the row holds x in dims 0..7 and zeros in 8..15, and
+// xbar = x / 8^(1/4) = x 2^-3/4 (one rounding to bf16); the d' = 8 map is then
+// the d' = 16 map of the padded row, restricted to the dims 0..7 (its other
+// features are zero): 16^(1/4) (2^(1/4) x) / 16^(1/4) = x 2^-3/4 per input,
+// so the feature values coincide.
+template <int kDk>
+__device__ __forceinline__ void xbar_pairs(const uint32_t (&raw)[8], uint32_t (&X)[8]) {
+    if constexpr (kDk == 16) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) X[j] = hmul2(raw[j], 0x3F003F00u);
+    } else {
+        static_assert(kDk == 8, "d' = 16 or 8");
+        constexpr float kS = 0.59460355750136053f;  // 2^-3/4
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(raw[j] << 16), hi = __uint_as_float(raw[j] & 0xFFFF0000u);
+            X[j] = pack_bf16(lo * kS, hi * kS);
+        }
+#pragma unroll
+        for (int j = 4; j < 8; ++j) X[j] = 0u;
+    }
+}
+
 // Feature vector of one token into its row of the feature tile; with kScaled
 // every feature is multiplied by scale2 (a bf16x2 pair of the same scale).
-template <bool kKey, bool kScaled = false, int... J>
+template <bool kKey, bool kScaled = false, int kDk = 16, int... J>
 __device__ __forceinline__ void emit_features(const uint4 &lo, const uint4 &hi, uint32_t base, int t,
                                               bool zero, std::integer_sequence<int, J...>,
                                               uint32_t scale2 = 0x3F803F80u) {
-    // xbar = x / 2 (exact), its odd-shifted pairs, and halves for the key squares
+    // xbar, its odd-shifted pairs, and halves for the key squares
     const uint32_t raw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     uint32_t X[8], Y[7], H[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) X[j] = hmul2(raw[j], 0x3F003F00u);
+    xbar_pairs<kDk>(raw, X);
 #pragma unroll
     for (int j = 0; j < 7; ++j) Y[j] = __byte_perm(X[j], X[j + 1], 0x5432);
 #pragma unroll
@@ -154,14 +177,13 @@ __device__ __forceinline__ void store_feature_group(const uint32_t (&XL)[8], con
     ((w[J] = feat_pair<kKey, 16 * G + J>(XL, X, Y, H, b15, cst)), ...);
     tmem_store16_sync(taddr + 16 * G, w);
 }
-template <bool kKey, bool kScaled = false, int... G>
+template <bool kKey, bool kScaled = false, int kDk = 16, int... G>
 __device__ __forceinline__ void emit_features_tmem(const uint4 &lo, const uint4 &hi, uint32_t taddr,
                                                    std::integer_sequence<int, G...>,
                                                    uint32_t scale2 = 0x3F803F80u) {
     const uint32_t raw[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     uint32_t X[8], Y[7], H[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) X[j] = hmul2(raw[j], 0x3F003F00u);
+    xbar_pairs<kDk>(raw, X);
 #pragma unroll
     for (int j = 0; j < 7; ++j) Y[j] = __byte_perm(X[j], X[j + 1], 0x5432);
 #pragma unroll
@@ -204,6 +226,33 @@ __host__ __device__ constexpr Rows abi_rows(int f) {
 }
 static_assert(abi_rows(0).r1 == 17 && abi_rows(152).r1 == 0 && abi_rows(153).kind == 3, "feature order");
 
+// The same for the state layout of d' = kDk (1 + kDk + kDk^2 rows; kDk = 8:
+// row 0 constant, 1 + a linear, 9 + 8 a + b quadratic).  At kDk = 8 the
+// features that involve dims 8..15 are zero and have no row (padding).
+template <int kDk>
+__host__ __device__ constexpr Rows abi_rows_t(int f) {
+    if (kDk == 16) return abi_rows(f);
+    const int r = f >> 1, e = f & 1;
+    const PairSpec p = pair_spec(r);
+    if (p.kind <= 2) {
+        int a = 0, b = 0;
+        pair_ab(r, e, a, b);
+        if (a >= kDk || b >= kDk) return {-1, -1, 3};
+        if (a == b) return {1 + kDk + (kDk + 1) * a, -1, 0};
+        return {1 + kDk + kDk * a + b, 1 + kDk + kDk * b + a, 1};
+    }
+    if (p.kind == 3) {
+        const int a = 2 * p.j + e;
+        return a < kDk ? Rows{1 + a, -1, 2} : Rows{-1, -1, 3};
+    }
+    if (p.kind == 4 && e == 0) return {0, -1, 2};
+    return {-1, -1, 3};
+}
+static_assert(abi_rows_t<8>(0).r1 == 9 && abi_rows_t<8>(152).r1 == 0 && abi_rows_t<8>(142).kind == 2 &&
+                  abi_rows_t<8>(142).r1 == 7 && abi_rows_t<8>(7).kind == 0 && abi_rows_t<8>(7).r1 == 72 &&
+                  abi_rows_t<8>(14).kind == 3 && abi_rows_t<8>(150).kind == 3,
+              "d' = 8 rows");
+
 // The conversions between the 273-row ABI state and the compact rows are
 // written per feature with the feature index F as a template argument, so the
 // kind and the ABI rows of every feature are compile-time constants (no row
@@ -211,9 +260,9 @@ static_assert(abi_rows(0).r1 == 17 && abi_rows(152).r1 == 0 && abi_rows(153).kin
 
 // Reads of the ABI column `col` (rows `stride` elements apart) that compact
 // feature F needs: its row, and for an off-diagonal pair the mirrored row.
-template <int F>
+template <int F, int kDk = 16>
 __device__ __forceinline__ void abi_reads(const float *col, int64_t stride, float &a, float &b) {
-    constexpr Rows e = abi_rows(F);
+    constexpr Rows e = abi_rows_t<kDk>(F);
     a = b = 0.f;
     if constexpr (e.kind != 3) a = __ldcg(col + e.r1 * stride);
     if constexpr (e.kind == 1) b = __ldcg(col + e.r2 * stride);
@@ -221,9 +270,9 @@ __device__ __forceinline__ void abi_reads(const float *col, int64_t stride, floa
 
 // Compact entry of feature F: squares carry 1/sqrt2, pairs the symmetric sum
 // over (a,b) and (b,a) times 1/sqrt2.
-template <int F>
+template <int F, int kDk = 16>
 __device__ __forceinline__ uint32_t compact_entry(float a, float b) {
-    constexpr Rows e = abi_rows(F);
+    constexpr Rows e = abi_rows_t<kDk>(F);
     if constexpr (e.kind == 3) return 0u;
     else if constexpr (e.kind == 2) return __float_as_uint(a);
     else if constexpr (e.kind == 0) return __float_as_uint(a * kRSqrt2);
@@ -233,7 +282,7 @@ __device__ __forceinline__ uint32_t compact_entry(float a, float b) {
 // Compact entries of the initial state for the 32 features of group G from
 // the ABI column `col` (NULL: zero state).  Every read is issued before any is
 // used, so they are in flight together.
-template <int G, int... J>
+template <int G, int kDk = 16, int... J>
 __device__ __forceinline__ void compact_initial_group(const float *col, int64_t stride, uint32_t (&r)[32],
                                                       std::integer_sequence<int, J...>) {
     if (!col) {
@@ -241,17 +290,17 @@ __device__ __forceinline__ void compact_initial_group(const float *col, int64_t 
         return;
     }
     float a[32], b[32];
-    (abi_reads<32 * G + J>(col, stride, a[J], b[J]), ...);
-    ((r[J] = compact_entry<32 * G + J>(a[J], b[J])), ...);
+    (abi_reads<32 * G + J, kDk>(col, stride, a[J], b[J]), ...);
+    ((r[J] = compact_entry<32 * G + J, kDk>(a[J], b[J])), ...);
 }
 
 // ABI value(s) of compact feature F with entry x: the rows' values, the
 // antisymmetric part anti (of a pair) added to (a,b) and subtracted from (b,a).
 // kStage: written into a shared-memory image at stage_d + 4 * 64 * row (value
 // column d: rows 256 bytes apart), else to out[row * stride] in global memory.
-template <bool kStage, int F>
+template <bool kStage, int F, int kDk = 16>
 __device__ __forceinline__ void abi_write(float x, float anti, uint32_t stage_d, float *out, int64_t stride) {
-    constexpr Rows e = abi_rows(F);
+    constexpr Rows e = abi_rows_t<kDk>(F);
     if constexpr (e.kind == 3) return;
     float v1, v2 = 0.f;
     if constexpr (e.kind == 2) v1 = x;
@@ -272,19 +321,19 @@ __device__ __forceinline__ void abi_write(float x, float anti, uint32_t stage_d,
 // One group G of the final ABI state from its compact entries r: the
 // antisymmetric part of the initial state's column col0 (NULL: none), scaled
 // by anti_scale, is read for the pairs (all reads issued together) and added.
-template <bool kStage, int G, int... J>
+template <bool kStage, int G, int kDk = 16, int... J>
 __device__ __forceinline__ void final_group(const uint32_t (&r)[32], const float *col0, int64_t stride,
                                             float anti_scale, uint32_t stage_d, float *out,
                                             std::integer_sequence<int, J...>) {
     float a[32], b[32];
     if (col0) {
-        (abi_reads<32 * G + J>(col0, stride, a[J], b[J]), ...);
+        (abi_reads<32 * G + J, kDk>(col0, stride, a[J], b[J]), ...);
     } else {
         ((a[J] = 0.f), ...);
         ((b[J] = 0.f), ...);
     }
     const float h = 0.5f * anti_scale;
-    (abi_write<kStage, 32 * G + J>(__uint_as_float(r[J]), h * (a[J] - b[J]), stage_d, out, stride), ...);
+    (abi_write<kStage, 32 * G + J, kDk>(__uint_as_float(r[J]), h * (a[J] - b[J]), stage_d, out, stride), ...);
 }
 
 // Drain wait used when unwinding: bounded, ignores the abort flag.
@@ -299,7 +348,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // the warp that owns lanes 64..95).  The value rows go to the shared-memory
 // image at `stage` (kStage, a [273][64] fp32 array) or to s_outh; z' goes to
 // z_outh.  A NULL destination is skipped.
-template <bool kStage, int G>
+template <bool kStage, int G, int kDk = 16>
 __device__ __forceinline__ void final_group_rows(uint32_t taddr, int d, bool zrow, int lane, const float *s0h,
                                                  uint32_t stage, float *s_outh, const float *z0h, float *z_outh,
                                                  float anti_scale) {
@@ -307,9 +356,9 @@ __device__ __forceinline__ void final_group_rows(uint32_t taddr, int d, bool zro
     uint32_t r[32];
     tmem_load32_sync(taddr + 32 * G, r);
     if (zrow) {
-        if (lane == 0 && z_outh) final_group<false, G>(r, z0h, 1, anti_scale, 0u, z_outh, js);
+        if (lane == 0 && z_outh) final_group<false, G, kDk>(r, z0h, 1, anti_scale, 0u, z_outh, js);
     } else if (kStage || s_outh) {
-        final_group<kStage, G>(r, s0h ? s0h + d : nullptr, kDV, anti_scale, stage + 4u * (uint32_t)d,
+        final_group<kStage, G, kDk>(r, s0h ? s0h + d : nullptr, kDV, anti_scale, stage + 4u * (uint32_t)d,
                                s_outh ? s_outh + d : nullptr, js);
     }
     __syncwarp();
@@ -317,11 +366,12 @@ __device__ __forceinline__ void final_group_rows(uint32_t taddr, int d, bool zro
 
 // Feature groups G0 + I... of the final ABI state (see final_group_rows).  Runs
 // once per CTA, so it is kept out of line.
-template <bool kStage, int G0, int... I>
+template <bool kStage, int G0, int kDk = 16, int... I>
 static __device__ __noinline__ void final_groups(uint32_t taddr, int d, bool zrow, int lane, const float *s0h,
                                                  uint32_t stage, float *s_outh, const float *z0h, float *z_outh,
                                                  float anti_scale, std::integer_sequence<int, I...>) {
-    (final_group_rows<kStage, G0 + I>(taddr, d, zrow, lane, s0h, stage, s_outh, z0h, z_outh, anti_scale), ...);
+    (final_group_rows<kStage, G0 + I, kDk>(taddr, d, zrow, lane, s0h, stage, s_outh, z0h, z_outh, anti_scale),
+     ...);
 }
 
 // ---- compact state layout in memory (153 rows: 0 constant, 1 + a linear,

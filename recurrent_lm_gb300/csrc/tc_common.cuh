@@ -382,9 +382,10 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 
 }  // namespace tc
 
-// [BH][N][width] bf16 rows as a 3-D TMA tensor map with a {width, 128, 1} box
-// (128-byte swizzle if swizzle128, else 32-byte); rows past N read as zero.
+// [BH][N][width] bf16 rows as a 3-D TMA tensor map with a {box_width, 128, 1}
+// box (box_width 0: width; 128-byte swizzle if swizzle128, else 32-byte); rows
+// past N, and columns past width, read as zero.
 bool make_row_tmap(CUtensorMap *map, const void *base, int64_t BH, int64_t N, int width,
-                   bool swizzle128, int box_rows = 128);
+                   bool swizzle128, int box_rows = 128, int box_width = 0);
 
 }  // namespace la

@@ -58,3 +58,36 @@ def test_general_dk_zero_length_copies_state():
     _, s, z = la.prefill(e, e, ev, s0.to(DEV), z0.to(DEV))
     torch.cuda.synchronize()
     assert torch.equal(s.cpu(), s0) and torch.equal(z.cpu(), z0)
+
+
+@pytest.mark.parametrize("N", [128, 1000, 4100])
+def test_dk8_tensor_core_prefill(N):
+    """bf16 at d' = 8 runs the tensor-core kernel on the padded map (q, k read
+    16 wide, the upper 8 columns zero): every chunk size class, a non-symmetric
+    initial state, against the oracle's d' = 8 map."""
+    D = oracle.feature_dim(8)
+    q, k, v, _, _ = inputs.qkv(2, 3, N, seed=1500 + N, dtype=torch.bfloat16, dk=8)
+    s0, z0 = inputs.random_state(2, 3, seed=1501, D=D)
+    got = la.prefill(q.to(DEV), k.to(DEV), v.to(DEV), s0.to(DEV), z0.to(DEV))
+    torch.cuda.synchronize()
+    la.check_device_status()
+    ref = oracle.prefill(q, k, v, s0, z0)
+    check(got, ref, TOL[torch.bfloat16], f" N={N}")
+
+
+def test_dk8_split_heads():
+    """d' = 8 with split heads (la_prefill_ws): every split head against the
+    oracle."""
+    B, H, N = 10, 16, 4096
+    r, _ = la.prefill_split_info(B, H, N)
+    assert r > 0
+    D = oracle.feature_dim(8)
+    q, k, v, _, _ = inputs.qkv(B, H, N, seed=1510, dtype=torch.bfloat16, dk=8)
+    s0, z0 = inputs.random_state(B, H, seed=1511, D=D)
+    y, s, z = la.prefill(q.to(DEV), k.to(DEV), v.to(DEV), s0.to(DEV), z0.to(DEV))
+    torch.cuda.synchronize()
+    la.check_device_status()
+    idx = list(range(B * H - r, B * H)) + [0]
+    sel = lambda t: torch.stack([t[i // H, i % H] for i in idx])[None]
+    ref = oracle.prefill(sel(q), sel(k), sel(v), sel(s0), sel(z0))
+    check((sel(y), sel(s), sel(z)), ref, TOL[torch.bfloat16])
