@@ -12,6 +12,11 @@
 // and accumulates phi(q)_r * s_r for the numerator.  Partial numerators are
 // summed across the 16 row groups in shared memory; the normaliser phi(q).z
 // uses a warp-shuffle reduction.
+//
+// Steps are launched with programmatic dependent launch, so a step's CTAs are
+// scheduled while the previous kernel in the stream drains; each waits for it
+// (griddepcontrol.wait) before reading anything, since that kernel may have
+// produced q, k, v or the state.
 #include "la_device.cuh"
 #include "la_internal.h"
 
@@ -39,6 +44,7 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
 
     const int64_t bh = blockIdx.x;
     const int tid = threadIdx.x;
+    pdl_wait();  // the previous kernel's outputs (q, k, v, the state) are complete from here on
     float g = 1.f;
     if constexpr (kDecay) {
         g = gamma[bh % H];
@@ -120,6 +126,7 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k,
         }
     }
     red[rg][cg] = acc;
+    pdl_trigger();  // this CTA's state is written; the next step may be scheduled
     __syncthreads();
 
     if (tid < kDV) {
@@ -143,17 +150,24 @@ cudaError_t launch_decode(const DecodeArgs &a, la_dtype dt, cudaStream_t st) {
     const int64_t BH = a.B * a.H;
     if (BH == 0) return cudaSuccess;
     dim3 grid((unsigned)BH), block(kThreads);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (dt == LA_DTYPE_BF16) {
         auto kern = a.gamma ? decode_step_kernel<__nv_bfloat16, true> : decode_step_kernel<__nv_bfloat16, false>;
-        kern<<<grid, block, 0, st>>>((const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k,
-                                     (const __nv_bfloat16 *)a.v, a.s_in, a.z_in, a.s_out, a.z_out,
-                                     (__nv_bfloat16 *)a.y, a.eps, a.gamma, a.H, a.status);
-    } else {
-        auto kern = a.gamma ? decode_step_kernel<float, true> : decode_step_kernel<float, false>;
-        kern<<<grid, block, 0, st>>>((const float *)a.q, (const float *)a.k, (const float *)a.v, a.s_in,
-                                     a.z_in, a.s_out, a.z_out, (float *)a.y, a.eps, a.gamma, a.H, a.status);
+        return cudaLaunchKernelEx(&cfg, kern, (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k,
+                                  (const __nv_bfloat16 *)a.v, a.s_in, a.z_in, a.s_out, a.z_out,
+                                  (__nv_bfloat16 *)a.y, a.eps, a.gamma, a.H, a.status);
     }
-    return cudaGetLastError();
+    auto kern = a.gamma ? decode_step_kernel<float, true> : decode_step_kernel<float, false>;
+    return cudaLaunchKernelEx(&cfg, kern, (const float *)a.q, (const float *)a.k, (const float *)a.v, a.s_in,
+                              a.z_in, a.s_out, a.z_out, (float *)a.y, a.eps, a.gamma, a.H, a.status);
 }
 
 }  // namespace la

@@ -13,7 +13,8 @@
 // The decode kernel has the structure of the 273-row one (one CTA per (b, h)
 // streams its state once with every load issued up front, float4 columns,
 // shared-memory row-group reduction of the numerator, warp shuffles for the
-// normaliser); per head it moves 39,168 B of s and 612 B of z each way.
+// normaliser); per head it moves 39,168 B of s and 612 B of z each way.  Steps
+// are launched with programmatic dependent launch (see decode.cu).
 #include "la_device.cuh"
 #include "la_internal.h"
 
@@ -58,6 +59,7 @@ decode_compact_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
 
     const int64_t bh = blockIdx.x;
     const int tid = threadIdx.x;
+    pdl_wait();  // the previous kernel's outputs (q, k, v, the state) are complete from here on
     if (tid < kDFeat) xq[tid] = 0.5f * Act<T>::load(q, bh * kDFeat + tid);
     else if (tid < 2 * kDFeat) xk[tid - kDFeat] = 0.5f * Act<T>::load(k, bh * kDFeat + tid - kDFeat);
 
@@ -114,6 +116,7 @@ decode_compact_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
         }
     }
     red[rg][cg] = acc;
+    pdl_trigger();  // this CTA's state is written; the next step may be scheduled
     __syncthreads();
 
     if (tid < kDV) {
@@ -212,15 +215,21 @@ unsigned conv_grid(int64_t work) {
 cudaError_t launch_decode_compact(const DecodeArgs &a, la_dtype dt, cudaStream_t st) {
     const int64_t BH = a.B * a.H;
     if (BH == 0) return cudaSuccess;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)BH);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (dt == LA_DTYPE_BF16)
-        decode_compact_kernel<__nv_bfloat16><<<(unsigned)BH, kThreads, 0, st>>>(
-            (const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, (const __nv_bfloat16 *)a.v, a.s_in, a.z_in,
-            a.s_out, a.z_out, (__nv_bfloat16 *)a.y, a.eps);
-    else
-        decode_compact_kernel<float><<<(unsigned)BH, kThreads, 0, st>>>(
-            (const float *)a.q, (const float *)a.k, (const float *)a.v, a.s_in, a.z_in, a.s_out, a.z_out,
-            (float *)a.y, a.eps);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&cfg, decode_compact_kernel<__nv_bfloat16>, (const __nv_bfloat16 *)a.q,
+                                  (const __nv_bfloat16 *)a.k, (const __nv_bfloat16 *)a.v, a.s_in, a.z_in, a.s_out,
+                                  a.z_out, (__nv_bfloat16 *)a.y, a.eps);
+    return cudaLaunchKernelEx(&cfg, decode_compact_kernel<float>, (const float *)a.q, (const float *)a.k,
+                              (const float *)a.v, a.s_in, a.z_in, a.s_out, a.z_out, (float *)a.y, a.eps);
 }
 
 cudaError_t launch_state_to_compact(const float *s, const float *z, float *s_c, float *z_c, int64_t BH,

@@ -27,6 +27,14 @@ template <> struct Act<__nv_bfloat16> {
     }
 };
 
+// Programmatic dependent launch (a launch with the programmatic stream
+// serialization attribute): pdl_wait blocks until the previous kernel in the
+// stream has completed and its memory is visible (a no-op without the
+// attribute); pdl_trigger lets the next kernel be scheduled once every CTA of
+// this grid has triggered or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 1/sqrt(2) rounded to fp32.
 constexpr float kInvSqrt2 = 0.70710678118654752440f;
 
