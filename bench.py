@@ -378,7 +378,7 @@ def decay_rates(H: int, dev) -> torch.Tensor:
 
 
 def leg_prefill_decay(la, args, dist, dev):
-    """The long-prefill workload with a fixed per-head decay (la_prefill_decay)."""
+    """The long-prefill workload with a fixed per-head decay (la_prefill_decay_ws)."""
     w = inputs.WORKLOADS[3]
     B, H, N = w.B, w.H, w.N
     g = torch.Generator(device=dev)
@@ -392,9 +392,12 @@ def leg_prefill_decay(la, args, dist, dev):
     y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
     s = torch.empty_like(s0)
     z = torch.empty_like(z0)
+    split = not args.no_split  # la_prefill_decay_ws: split heads of the last wave
+    need = la.load_library().la_prefill_workspace_size(B, H, N, 16, la.binding.LA_DTYPE_BF16)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev) if split else None
 
     def step():
-        la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z, gamma=gam)
+        la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z, gamma=gam, workspace=ws, split=split)
 
     ms = time_loop(step, max(1, args.steps // 2), max(3, args.warmup // 2), dist)
     la.check_device_status()

@@ -277,6 +277,16 @@ LA_API la_status la_prefill_decay(const void *q, const void *k, const void *v,
                                   int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
                                   la_dtype dtype, float eps, la_stream_t stream);
 
+/* la_prefill_decay with the workspace of la_prefill_ws (split heads of the last
+ * wave; la_prefill_workspace_size gives its size).  NULL or too small a
+ * workspace runs exactly la_prefill_decay. */
+LA_API la_status la_prefill_decay_ws(const void *q, const void *k, const void *v,
+                                     const float *s0, const float *z0, const float *gamma,
+                                     void *y, float *s_out, float *z_out,
+                                     void *workspace, size_t workspace_bytes,
+                                     int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                                     la_dtype dtype, float eps, la_stream_t stream);
+
 LA_API la_status la_decode_step_decay(const void *q, const void *k, const void *v,
                                       const float *gamma, const float *s_in, const float *z_in,
                                       float *s_out, float *z_out, void *y,

@@ -53,6 +53,8 @@ SIGNATURES = {
     "la_prefix_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "la_prefill_host_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _I]),
     "la_prefill_workspace_size": (_SZ, [_I64, _I64, _I64, _I, _I]),
+    "la_prefill_decay_ws": (_I, [_VP, _VP, _VP, _FP, _FP, _FP, _VP, _FP, _FP, _VP, _SZ, _I64, _I64, _I64,
+                                 _I, _I, _I, _F, _VP]),
     "la_prefill_split_info": (_I, [_I64, _I64, _I64, ctypes.POINTER(ctypes.c_int),
                                    ctypes.POINTER(ctypes.c_int)]),
     "la_prefill_ws": (_I, [_VP, _VP, _VP, _FP, _FP, _VP, _FP, _FP, _VP, _SZ, _I64, _I64, _I64, _I, _I,
@@ -192,9 +194,16 @@ def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
         if left_pad is not None:
             raise ValueError("left_pad and gamma cannot be combined")
         _need(gamma, "gamma", (H,), torch.float32)
-        _raise(lib.la_prefill_decay(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(gamma),
-                                    _ptr(y), _ptr(s_out), _ptr(z_out), B, H, N, dk, D_V, _dt(q),
-                                    float(eps), _stream(stream)))
+        need = int(lib.la_prefill_workspace_size(B, H, N, dk, _dt(q))) if split else 0
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            _keep_for(workspace, stream)
+        if workspace is not None:
+            _need(workspace, "workspace", (workspace.numel(),), torch.uint8)
+        _raise(lib.la_prefill_decay_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(s0), _ptr(z0), _ptr(gamma),
+                                       _ptr(y), _ptr(s_out), _ptr(z_out), _ptr(workspace),
+                                       0 if workspace is None else workspace.numel(), B, H, N, dk, D_V,
+                                       _dt(q), float(eps), _stream(stream)))
     elif left_pad is None:
         # la_prefill_ws with a workspace from torch's caching allocator (it
         # balances the last wave of heads on the bf16 path); la_prefill when

@@ -247,7 +247,7 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
     la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad, gamma};
     a.compact = compact;
     // split heads on the bf16 tensor-core path, given room for the hand-over
-    if (workspace && dtype == LA_DTYPE_BF16 && (d_feat == kDFeat || d_feat == 8) && !gamma &&
+    if (workspace && dtype == LA_DTYPE_BF16 && (d_feat == kDFeat || d_feat == 8) &&
         workspace_bytes >= xfer_bytes(BH) + xflag_bytes(BH))
         plan_split(a, dev, static_cast<char *>(workspace));
     return to_status(run_prefill(a, dtype, reinterpret_cast<cudaStream_t>(stream), d_feat));
@@ -354,6 +354,15 @@ la_status la_prefill_ws(const void *q, const void *k, const void *v, const float
                         int64_t N, int d_feat, int d_v, la_dtype dtype, float eps, la_stream_t stream) {
     return prefill_impl(q, k, v, s0, z0, nullptr, y, s_out, z_out, B, H, N, d_feat, d_v, dtype, eps, stream,
                         nullptr, false, workspace, workspace ? workspace_bytes : 0);
+}
+
+la_status la_prefill_decay_ws(const void *q, const void *k, const void *v, const float *s0, const float *z0,
+                              const float *gamma, void *y, float *s_out, float *z_out, void *workspace,
+                              size_t workspace_bytes, int64_t B, int64_t H, int64_t N, int d_feat, int d_v,
+                              la_dtype dtype, float eps, la_stream_t stream) {
+    if (!gamma) return LA_ERR_INVALID_ARG;
+    return prefill_impl(q, k, v, s0, z0, nullptr, y, s_out, z_out, B, H, N, d_feat, d_v, dtype, eps, stream,
+                        gamma, false, workspace, workspace ? workspace_bytes : 0);
 }
 
 la_status la_prefill_padded(const void *q, const void *k, const void *v, const float *s0,

@@ -427,8 +427,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     }
     // length of chunk c (the last may be short)
     auto chunk_len = [&](int c) { return min(kC, N - (c0 + c) * kC); };
-    // the antisymmetric part of s0 bypasses the compact state: it decays by gamma^N
-    const float anti_decay = kDecay ? powf(pow_gamma(1), (float)N) : 1.f;
+    // the antisymmetric part of the initial state bypasses the compact state: it
+    // decays by gamma to the number of tokens this CTA covers (N for a whole
+    // head; a split head's pieces hand it over through the transfer slot)
+    const float anti_decay =
+        kDecay ? powf(pow_gamma(1), (float)(min(N, (c0 + n) * kC) - c0 * kC)) : 1.f;
 
     // the first kStages chunks' loads (their stages start empty) go out now, so
     // that they land while the initial state is read; warp 3 has no state rows

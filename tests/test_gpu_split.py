@@ -100,7 +100,7 @@ def test_split_prefix_prefill(padded):
     pad = None
     if padded:
         pad = torch.from_numpy(np.random.default_rng(4302).integers(0, N + 1, size=B).astype(np.int32))
-        pad[-1] = 7000  # the last row's first pieces (split at about 11 chunks) are all padding
+        pad[-1] = 7000  # the last row's first pieces (8 chunks at this size) are all padding
     dev = [t.to(DEV) for t in (q, k, v, ke, ve, s0, z0)]
     got = la.prefix_prefill(*dev, left_pad=None if pad is None else pad.to(DEV))
     torch.cuda.synchronize()
@@ -120,3 +120,28 @@ def test_split_prefix_prefill(padded):
                                         left_pad=[lp[j]])
             for name, a, rr in zip("ysz", got, ref):
                 assert_close(f"{name} head {i}", a[i // H, i % H][None, None], rr, TOL[torch.bfloat16])
+
+
+def test_split_decayed_prefill():
+    """The decayed prefill splits the same way (la_prefill_decay_ws): every
+    split head against the oracle, with per-head rates from 1 down to 0.5 and
+    a non-symmetric s0, whose antisymmetric part the pieces hand over decayed
+    by their own lengths."""
+    B, H, N = 16, 16, 8192
+    r, _ = la.prefill_split_info(B, H, N)
+    assert r > 0
+    q, k, v, _, _ = inputs.qkv(B, H, N, seed=4400, dtype=torch.bfloat16)
+    s0, z0 = inputs.random_state(B, H, seed=4401, tokens=128.0)
+    g = [1.0 - 2.0 ** -(4 + h) for h in range(H - 2)] + [1.0, 0.5]
+    g32 = torch.tensor(g, dtype=torch.float32)
+    got = la.prefill(q.to(DEV), k.to(DEV), v.to(DEV), s0.to(DEV), z0.to(DEV), gamma=g32.to(DEV))
+    torch.cuda.synchronize()
+    la.check_device_status()
+    BH = B * H
+    idx = sorted(set(range(BH - r, BH, 2)) | {BH - 1, BH - r, 0})
+    for i in idx:
+        b, h = i // H, i % H
+        one = lambda t: t[b, h][None, None]
+        ref = oracle.prefill_decay(one(q), one(k), one(v), g32[h:h + 1].double().numpy(), one(s0), one(z0))
+        for name, a, rr in zip("ysz", got, ref):
+            assert_close(f"{name} head {i}", a[b, h][None, None], rr, TOL[torch.bfloat16])
