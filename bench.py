@@ -209,27 +209,32 @@ class Clocks:
                 "power_w_median": statistics.median(watts) if watts else None}
 
 
+LAST_MEDIAN_MS = [None]   # median per-step time of the last time_loop (this rank)
+
+
 def time_loop(fn, steps, warmup, dist):
-    """Run fn() warmup times untimed, then `steps` times between events on the
-    current stream; returns ms per step (max over ranks)."""
+    """Run fn() warmup times untimed, then `steps` times with an event on the
+    current stream before each step and after the last; returns the mean ms per
+    step (max over ranks) and leaves the median step in LAST_MEDIAN_MS."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     t0 = time.time()
-    e0.record(st)
-    for _ in range(steps):
+    for i in range(steps):
+        ev[i].record(st)
         fn()
-    e1.record(st)
-    e1.synchronize()
+    ev[steps].record(st)
+    ev[steps].synchronize()
     torch.cuda.synchronize()
     TIMED_WINDOWS.append((t0, time.time()))
     dist.barrier()
-    return dist.max(e0.elapsed_time(e1) / steps)
+    per = sorted(ev[i].elapsed_time(ev[i + 1]) for i in range(steps))
+    LAST_MEDIAN_MS[0] = per[steps // 2] if steps % 2 else 0.5 * (per[steps // 2 - 1] + per[steps // 2])
+    return dist.max(ev[0].elapsed_time(ev[steps]) / steps)
 
 
 def shard_seed(seed: int, rank: int) -> int:
@@ -267,9 +272,10 @@ def leg_prefill(la, args, dist, dev, clocks):
         la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z, workspace=ws, split=split)
 
     ms = time_loop(step, args.steps, args.warmup, dist)
+    ms_median = LAST_MEDIAN_MS[0]
     la.check_device_status()
     r, n1 = la.prefill_split_info(B, H, N) if split else (0, 0)
-    out = {"ms": ms, "B": B, "H": H, "N": N, "split_heads": r, "split_chunk": n1,
+    out = {"ms": ms, "ms_median": ms_median, "B": B, "H": H, "N": N, "split_heads": r, "split_chunk": n1,
            "finite": bool(torch.isfinite(y[:, :, -1].float()).all().item())}
     if not args.no_e2e:
         out["e2e"] = e2e_prefill(la, args, dist, q, k, v, s0, z0)
@@ -631,6 +637,7 @@ def main():
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": pre["ms"],
+        "ms_per_step_median": pre["ms_median"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
