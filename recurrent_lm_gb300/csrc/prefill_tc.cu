@@ -80,8 +80,11 @@ constexpr uint32_t kSmQ = 182272;      // 3 x [128][16] bf16 SW32
 constexpr uint32_t kSmK = 194560;      // 3 x [128][16] bf16 SW32
 constexpr uint32_t kSmY = 206848;      // 4 x [32 rows][64] bf16 SW128: y staging for TMA stores
 constexpr uint32_t kSmBar = kSmY + 16384;
-constexpr uint32_t kSmPow = kSmBar + 512;  // decay: [129] float2 (gamma^d, gamma^(d-1))
-constexpr uint32_t kSmTotal = kSmPow + 1280;
+// decay: [129] float2 (gamma^d, gamma^(d-1)), then at kPowInvOff [32] float2
+// (gamma^-2j, gamma^-2j)
+constexpr uint32_t kSmPow = kSmBar + 512;
+constexpr uint32_t kPowInvOff = 1040;
+constexpr uint32_t kSmTotal = kSmPow + kPowInvOff + 256;
 constexpr uint32_t kSmAlloc = kSmTotal + 1024;
 constexpr int kStages = 3;
 
@@ -182,22 +185,49 @@ static __device__ __noinline__ bool p_block(uint32_t tsrc, uint32_t tdst, int pp
         const uint64_t c32 = f2pack(kQuad, kQuad), c4 = f2pack(kLin, kLin), c1 = f2pack(1.0f, 1.0f);
         const bool diag = 64 * pp + 63 >= 32 * w;  // this block reaches the diagonal
         if constexpr (kDecay) {
-            // times the decay factors (gamma^(i-j), gamma^(i-j-1)) from the power
-            // table; j > i is masked below
+            // times the decay factors gamma^(i-key) (key > i is masked below)
             uint32_t r[64];
             tmem_load64_sync(tsrc + 64 * pp, r);
+            if (__uint_as_float((uint32_t)ld_shared_u64(pow + 8u)) >= 0.25f) {
+                // separable within the block: gamma^(i-key) = gamma^(i-64pp) gamma^(-2j)
+                // for the key pair 64pp + 2j, +1.  The row's factor scales the
+                // polynomial's coefficients; the key's factor (warp-uniform, a
+                // broadcast read, below 2^124 for gamma >= 1/4) multiplies P.
+                const uint64_t a2 = ld_shared_u64(pow + 8u * (uint32_t)(i - 64 * pp));  // i >= 64 pp
+                const uint64_t e1 = a2, e4 = fmul2(c4, a2), e32 = fmul2(c32, a2);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int key = 64 * pp + 2 * j;
-                const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
-                const uint64_t f2 = ld_shared_u64(pow + 8u * (uint32_t)max(i - key, 0));
-                const uint64_t p2 = fmul2(ffma2(t2, ffma2(t2, c32, c4), c1), f2);
-                float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
-                if (diag) {
-                    if (key > i) p0 = 0.f;
-                    if (key + 1 > i) p1 = 0.f;
+                for (int j2 = 0; j2 < 16; ++j2) {
+                    const uint4 u = ld_shared_v4(pow + kPowInvOff + 16u * (uint32_t)j2);  // (gamma^-2j) x 2, j = 2 j2, +1
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = 2 * j2 + h, key = 64 * pp + 2 * j;
+                        const uint64_t uj = h ? ((uint64_t)u.z | ((uint64_t)u.w << 32))
+                                              : ((uint64_t)u.x | ((uint64_t)u.y << 32));
+                        const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
+                        const uint64_t p2 = fmul2(ffma2(t2, ffma2(t2, e32, e4), e1), uj);
+                        float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
+                        if (diag) {
+                            if (key > i) p0 = 0.f;
+                            if (key + 1 > i) p1 = 0.f;
+                        }
+                        pw[j] = pack_bf16(p0, p1);
+                    }
                 }
-                pw[j] = pack_bf16(p0, p1);
+            } else {
+                // small rates: (gamma^(i-key), gamma^(i-key-1)) from the power table
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int key = 64 * pp + 2 * j;
+                    const uint64_t t2 = (uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32);
+                    const uint64_t f2 = ld_shared_u64(pow + 8u * (uint32_t)max(i - key, 0));
+                    const uint64_t p2 = fmul2(ffma2(t2, ffma2(t2, c32, c4), c1), f2);
+                    float p0 = __uint_as_float((uint32_t)p2), p1 = __uint_as_float((uint32_t)(p2 >> 32));
+                    if (diag) {
+                        if (key > i) p0 = 0.f;
+                        if (key + 1 > i) p1 = 0.f;
+                    }
+                    pw[j] = pack_bf16(p0, p1);
+                }
             }
         } else {
             uint32_t r[64];
@@ -423,6 +453,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         if (tid <= 128)
             reinterpret_cast<float2 *>(smem + kSmPow)[tid] =
                 make_float2(powf(g, (float)tid), tid > 0 ? powf(g, (float)(tid - 1)) : 0.f);
+        else if (tid >= 160 && tid < 192) {  // read only for gamma >= 1/4 (finite there)
+            const float u = powf(g, -2.f * (float)(tid - 160));
+            reinterpret_cast<float2 *>(smem + kSmPow + kPowInvOff)[tid - 160] = make_float2(u, u);
+        }
         __syncthreads();
     }
     // length of chunk c (the last may be short)

@@ -58,6 +58,22 @@ def test_decayed_prefill_across_epochs(N):
     check(got, ref, TOL[torch.bfloat16], f" N={N}")
 
 
+@pytest.mark.parametrize("N", [333, 1000])
+def test_decayed_prefill_small_rates(N):
+    """bf16 decayed prefill with rates on both sides of 1/4, where the
+    intra-chunk factors change from a per-row times per-key product to a
+    power-table read, down to 0 (each token sees only itself): against the
+    oracle, ragged N."""
+    g = [0.26, 0.25, 0.2499, 0.1, 0.01, 0.0, 1.0, 0.4]
+    q, k, v, _, _ = inputs.qkv(1, len(g), N, seed=1160 + N, dtype=torch.bfloat16)
+    s0, z0 = inputs.random_state(1, len(g), seed=1161)
+    g32 = torch.tensor(g, dtype=torch.float32)
+    got = la.prefill(q.to(DEV), k.to(DEV), v.to(DEV), s0.to(DEV), z0.to(DEV), gamma=g32.to(DEV))
+    la.check_device_status()
+    ref = oracle.prefill_decay(q, k, v, g32.double().numpy(), s0, z0)
+    check(got, ref, TOL[torch.bfloat16], f" N={N}")
+
+
 def test_decay_of_one_is_the_plain_prefill():
     q, k, v, _, _ = inputs.qkv(2, 3, 700, seed=1110)
     s0, z0 = inputs.random_state(2, 3, seed=1111)
