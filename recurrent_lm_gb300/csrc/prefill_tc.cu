@@ -154,14 +154,14 @@ __device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, i
             write_sb_group(sbase, zrow ? 64 : d, kG0 + g, *reinterpret_cast<const uint32_t (*)[32]>(r + 32 * g));
     }
     if constexpr (kDecay) {
+        // rescaled in place and written back with one store and one wait
         __syncwarp();  // tcgen05.st is warp-collective
 #pragma unroll
-        for (int g = 0; g < kNG; ++g) {
-            uint32_t w[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(__uint_as_float(r[32 * g + j]) * decay);
-            tmem_store32_sync(taddr + 32 * (kG0 + g), w);
-        }
+        for (int j = 0; j < 32 * kNG; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * decay);
+        if constexpr (kNG == 2)
+            tmem_store64_sync(taddr + 32 * kG0, reinterpret_cast<const uint32_t (&)[64]>(r));
+        else
+            tmem_store32_sync(taddr + 32 * kG0, reinterpret_cast<const uint32_t (&)[32]>(r));
     }
 }
 
