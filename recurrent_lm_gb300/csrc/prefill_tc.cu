@@ -713,12 +713,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             if (c > 0 && tid == 128) LA_TR(TR_CONV, c - 1, 2);
             if (c > 0 && tid == 128) mbar_arrive(bar(B_V_EMPTY + (c - 1) % kStages));
             if (c > 0) {
-                // state after chunk c - 1, feature groups 3, 4 -> operand of the read-out of c
+                // state after chunk c - 1, feature groups 3, 4 (with decay only 4: the
+                // rescale would hold up the key features below) -> operand of the
+                // read-out of c
                 __syncwarp();
                 tc_fence_after();
-                if (wq < 3)
-                    convert_groups<3, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, 32 * wq + lane, zrow, lane,
-                                                 pow_gamma(chunk_len(c)));
+                if (wq < 3) {
+                    if constexpr (kDecay)
+                        convert_groups<4, 1, true>(tmem + lanebase + kTmS, sb + kSmSb, 32 * wq + lane, zrow, lane,
+                                                   pow_gamma(chunk_len(c)));
+                    else
+                        convert_groups<3, 2, false>(tmem + lanebase + kTmS, sb + kSmSb, 32 * wq + lane, zrow, lane);
+                }
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -817,7 +823,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     const float dn = pow_gamma(chunk_len(c + 1));
                     convert_groups<0, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                     __syncwarp();
-                    convert_groups<2, 1, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
+                    if constexpr (kDecay) {  // groups 2, 3 (the feature warps keep only group 4)
+                        convert_groups<2, 1, true>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
+                        __syncwarp();
+                        convert_groups<3, 1, true>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
+                    } else
+                        convert_groups<2, 1, false>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                 } else if constexpr (kCompact) {
                     final_groups_compact<true, 0>(tmem + lanebase + kTmS, i, zrow, lane, sb + kSmStage, s_outh,
                                                   z_outh, std::make_integer_sequence<int, 3>{});
