@@ -412,7 +412,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
         mbar_init(bar(B_T_FULL), 1);
-        mbar_init(bar(B_PV_READY), 6 + 4);  // P warps 8..11, 2, 3; y warps
+        // P warps 8..11, 2, 3; y warps (with decay the y warps write P of keys
+        // 0..63 instead of warps 8..11)
+        mbar_init(bar(B_PV_READY), (kDecay ? 2 : 6) + 4);
         mbar_init(bar(B_RO_READY), 4 + 8);
         mbar_init(bar(B_PHK_FULL), 4);
         mbar_init(bar(B_NUM_FULL), 1);
@@ -718,13 +720,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                 // read-out of c
                 __syncwarp();
                 tc_fence_after();
-                if (wq < 3) {
-                    if constexpr (kDecay)
-                        convert_groups<4, 1, true>(tmem + lanebase + kTmS, sb + kSmSb, 32 * wq + lane, zrow, lane,
-                                                   pow_gamma(chunk_len(c)));
-                    else
+                if constexpr (!kDecay)
+                    if (wq < 3)
                         convert_groups<3, 2, false>(tmem + lanebase + kTmS, sb + kSmSb, 32 * wq + lane, zrow, lane);
-                }
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
@@ -782,7 +780,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
         const bool zrow = (w == 2);  // warp 10: lane 64 holds z'
         // rows 0..63 see no key of 64..127: their P columns 32..63 stay zero
-        if (w < 2) {
+        // (with decay the y warps write them, before their first arrival)
+        if (!kDecay && w < 2) {
             uint32_t zero[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) zero[j] = 0u;
@@ -809,10 +808,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // After P(c + 1) (done well before the update of chunk c completes), the
         // state after chunk c, feature groups 0..2: the operand of the read-out of
         // chunk c + 1, or the final state (groups 3, 4: gen warps).
+        // (With decay the y warps take the P blocks: these warps only convert.)
         if (lane == 0) mbar_arrive(bar(B_RO_READY));  // phase 0: initial operand written in set-up
-        bool ok = do_p(0);
+        bool ok = kDecay ? true : do_p(0);
         for (int c = 0; ok && c < n; ++c) {
-            if (c + 1 < n && !(ok = do_p(c + 1))) break;
+            if (!kDecay && c + 1 < n && !(ok = do_p(c + 1))) break;
             if (!(ok = mbar_wait(bar(B_S_FULL), (uint32_t)c & 1u, abort, status))) break;
             if (tid == 256) LA_TR(TR_CONV, c, 0);
             __syncwarp();
@@ -827,6 +827,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                         convert_groups<2, 1, true>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                         __syncwarp();
                         convert_groups<3, 1, true>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
+                        __syncwarp();
+                        convert_groups<4, 1, true>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                     } else
                         convert_groups<2, 1, false>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                 } else if constexpr (kCompact) {
@@ -866,11 +868,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     (c + 1 >= n || mbar_wait(bar(B_QK_FULL + (c + 1) % kStages), (uint32_t)((c + 1) / kStages) & 1u,
                                              abort, status)));
         };
+        // With decay these warps also form P of keys 0..63 for their rows (the
+        // P warps' role without decay): P(c + 1) once Q K^T(c + 1) is in T, stored
+        // once P V(c) has completed (NUM_FULL(c)), before num(c) is drained, so
+        // that one arrival covers both.
+        auto p_next = [&](int c) -> bool {  // P(c)
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_T_FULL), (uint32_t)c & 1u, abort, status))) return false;
+            if (tid == 384) mbar_arrive(bar(B_QK_EMPTY + c % kStages));  // Q K^T(c) has read its q, k stage
+            tc_fence_after();
+            return p_block<kPad, kDecay, kDk>(tmem + lanebase + kTmT, tmem + lanebase + kTmP, 0, i, w,
+                                              kPad ? lpad - (c0 + c) * kC : 0, sb + kSmPow,
+                                              c > 0 ? bar(B_NUM_FULL) : 0u, (uint32_t)(c - 1) & 1u, abort, status);
+        };
         bool ok = __all_sync(0xffffffffu, observe(0));
-        if (ok && lane == 0) mbar_arrive(bar(B_PV_READY));  // phase 0: num starts drained
+        if constexpr (kDecay) {
+            if (w < 2) {  // rows 0..63 see no key of 64..127: their P columns 32..63 stay zero
+                uint32_t zero[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) zero[j] = 0u;
+                tmem_store32_sync(tmem + lanebase + kTmP + 32, zero);
+            }
+            ok = ok && p_next(0);
+            tc_fence_before();
+            __syncwarp();
+        }
+        if (ok && lane == 0) mbar_arrive(bar(B_PV_READY));  // phase 0: num starts drained (with decay: P(0))
         for (int c = 0; ok && c < n; ++c) {
             // ---- y(c)
             const bool seen = observe(c + 1);
+            if constexpr (kDecay)
+                if (c + 1 < n && !p_next(c + 1)) break;
             if (!mbar_wait(bar(B_NUM_FULL), (uint32_t)c & 1u, abort, status)) break;
             if (tid == 384) LA_TR(TR_EPI, c, 2);
             __syncwarp();
