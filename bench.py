@@ -515,7 +515,8 @@ def ncu_case(la, case: str):
     compact state) at the bench batch B=128, H=16, ten steps in place back to
     back (inputs generated first, so that nothing runs between the steps; the
     compact case over the bench leg's independent states in turn);
-    prefix N=M=4096, three calls."""
+    prefix N=M=4096, three calls; the decayed prefill (the bench leg's rates)
+    at B=16, H=16, N=8192 with an initial state, two launches (split heads)."""
     dev = "cuda:0"
     g = torch.Generator(device=dev)
     g.manual_seed(0)
@@ -547,6 +548,16 @@ def ncu_case(la, case: str):
         for i in range(T):
             for s, z in states:
                 step(q[i], k[i], v[i], s, z, y=y[i], inplace=True)
+    elif case == "prefill_decay":
+        B, H, N = 16, 16, 8192
+        s0 = torch.randn(B, H, 273, 64, device=dev, generator=g)
+        z0 = torch.rand(B, H, 273, device=dev, generator=g) + 64.0
+        q = gen_device((B, H, N, 16), g, dev=dev)
+        k = gen_device((B, H, N, 16), g, dev=dev)
+        v = gen_device((B, H, N, 64), g, dev=dev)
+        gam = decay_rates(H, dev)
+        for _ in range(2):
+            la.prefill(q, k, v, s0, z0, gamma=gam)
     elif case == "prefix":
         B, H, N, M = 16, 16, 4096, 4096
         q, k = gen_device((B, H, N, 16), g, dev=dev), gen_device((B, H, N, 16), g, dev=dev)
@@ -577,7 +588,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-split", action="store_true",
                     help="time la_prefill without the workspace (no split heads in the last wave)")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_compact", "prefix"],
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_compact", "prefix", "prefill_decay"],
                     help="run one small case for an ncu capture and exit (no timing)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
