@@ -35,7 +35,9 @@
 //    (TMEM fp32 -> bf16 operand) of feature groups 3, 4, warpgroup 2 the P
 //    epilogue of keys 0..63 and the conversion of groups 0..2, warpgroup 3
 //    the output epilogue y = num / den (TMA stores).  The final state is
-//    assembled in shared memory and written with one bulk copy.
+//    assembled in shared memory and written with one bulk copy.  With decay
+//    the y warps also form P of keys 0..63, warpgroup 2 converts (and
+//    rescales) all five groups, and the feature warps only emit features.
 //  * Every wait is bounded: after ~1 s the kernel records a timeout in the
 //    device status word and every role unwinds.
 #include <type_traits>
@@ -167,13 +169,13 @@ __device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, i
 
 // P = 1 + T/4 + T^2/32 for the keys 64 pp .. 64 pp + 63 of query row i (TMEM
 // lane quarter w, 2 pp <= w), with the causal mask (key > i), left padding
-// (key < kmin) and, with decay, the factor gamma^(i - key) from the power
-// table at `pow`.  Reads T at `tsrc` + 64 pp; once the previous chunk's P V
-// has read the P buffer (phase `wpar` of the barrier `wbar`; wbar = 0: no
-// wait) writes the 32 packed bf16 columns to `tdst`.  Returns false if that
-// wait gave up.  Kept out of line: the six P warps share one copy of this
-// code (the kernel's roles together run more code than the instruction cache
-// holds).
+// (key < kmin) and, with decay, the factor gamma^(i - key) from the tables at
+// `pow` (powers gamma^d, and gamma^-2j at kPowInvOff).  Reads T at `tsrc` +
+// 64 pp; once the previous chunk's P V has read the P buffer (phase `wpar` of
+// the barrier `wbar`; wbar = 0: no wait) writes the 32 packed bf16 columns to
+// `tdst`.  Returns false if that wait gave up.  Kept out of line: the warps
+// that form P share one copy of this code (the kernel's roles together run
+// more code than the instruction cache holds).
 template <bool kPad, bool kDecay, int kDk = 16>
 static __device__ __noinline__ bool p_block(uint32_t tsrc, uint32_t tdst, int pp, int i, int w, int kmin,
                                             uint32_t pow, uint32_t wbar, uint32_t wpar, volatile int *abort,
