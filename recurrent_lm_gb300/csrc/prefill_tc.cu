@@ -825,7 +825,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     const float dn = pow_gamma(chunk_len(c + 1));
                     convert_groups<0, 2, kDecay>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                     __syncwarp();
-                    if constexpr (kDecay) {  // groups 2, 3 (the feature warps keep only group 4)
+                    if constexpr (kDecay) {  // with decay these warps convert every group
                         convert_groups<2, 1, true>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
                         __syncwarp();
                         convert_groups<3, 1, true>(tmem + lanebase + kTmS, sb + kSmSb, i, zrow, lane, dn);
