@@ -97,7 +97,10 @@ enum {
     // PV_READY(c): P(c) (P warps) and num drained after chunk c - 1 (y warps);
     // RO_READY(c): Phi'_Q(c) (gen warps) and the state operand after chunk c - 1
     // (conversion warps).  Merged so the MMA issuer waits once for each: its
-    // waits are expensive after MMA issue.
+    // waits are expensive after MMA issue.  With decay RO_READY(c) also covers
+    // Phi'_K(c) (PHK_FULL is unused there): one wait fewer per chunk, which pays
+    // in the decayed kernel, whose issuer is not its bottleneck, and not in
+    // the plain one, where the update's operand lands after the read-out's.
     B_PV_READY = 14, B_RO_READY, B_PHK_FULL,
     B_NUM_FULL, B_S_FULL, B_FINAL,
     B_STAGED,   // the final state's value rows are in the shared-memory image
@@ -417,7 +420,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         // P warps 8..11, 2, 3; y warps (with decay the y warps write P of keys
         // 0..63 instead of warps 8..11)
         mbar_init(bar(B_PV_READY), (kDecay ? 2 : 6) + 4);
-        mbar_init(bar(B_RO_READY), 4 + 8);
+        // P warps; gen warps twice (Phi'_Q, conversion), with decay three times (+ Phi'_K)
+        mbar_init(bar(B_RO_READY), 4 + (kDecay ? 12 : 8));
         mbar_init(bar(B_PHK_FULL), 4);
         mbar_init(bar(B_NUM_FULL), 1);
         mbar_init(bar(B_S_FULL), 1);
@@ -638,8 +642,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                     mma_bf16_ts_warp(tmem + kTmNum, tmem + kTmPhiQ + 8 * s, db, kIdRO, 1);
                 }
                 mma_commit_warp(bar(B_NUM_FULL));  // also: Phi'_Q and the P buffer free
-                // state update operand Phi'_K(c)
-                if (!(ok = wwait(bar(B_PHK_FULL), pc))) break;
+                // state update operand Phi'_K(c) (with decay part of RO_READY(c))
+                if (!kDecay && !(ok = wwait(bar(B_PHK_FULL), pc))) break;
                 if (lane == 0) LA_TR(TR_MMA, c, 3);
                 tc_fence_after();
                 // state update: [S'^T ; z'] += [V | 1]^T Phi'_K, 16 tokens per MMA
@@ -740,7 +744,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             }
             fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PHK_FULL));
+            if (lane == 0) mbar_arrive(bar(kDecay ? B_RO_READY : B_PHK_FULL));
             if (tid == 128) LA_TR(TR_GEN, c, 3);
             if (c == n - 1) gen_done = true;
         }
