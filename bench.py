@@ -12,8 +12,9 @@ times the other two calls of the path, reported under ``legs``:
     twice (2N = 65536 tokens), timed against the prefix call;
   - prefill_decay / decode_decay: the long-prefill and decode workloads with a
     fixed per-head decay 1 - 2^-(4+h) (la_prefill_decay, la_decode_step_decay);
-  - prefill_dk8/24/32: la_prefill on the general feature-dimension path
-    (B=4, H=16, N=4096);
+  - prefill_dk8/24/32: la_prefill_ws at other feature dimensions (d' = 8 on
+    the tensor-core kernel at the long-prefill shape; d' = 24, 32 at B=4,
+    H=16, N=4096 with cuBLASLt batched GEMMs and 4 kernels of the library);
   - decode: la_decode_step on B=128, H=16, 512 consecutive steps captured in
     one CUDA graph, state from a 2048-token prefill (tokens/s and HBM GB/s).
 Inputs are seeded synthetic tensors already resident in HBM and larger than
@@ -411,9 +412,11 @@ def leg_prefill_decay(la, args, dist, dev):
 
 
 def leg_general_dk(la, args, dist, dev):
-    """la_prefill at other feature dimensions, bf16, with an initial state:
-    d' = 8 on the tensor cores (the padded map) at the long-prefill shape B=16,
-    H=16, N=32768; d' = 24, 32 on the CUDA-core path at B=4, H=16, N=4096."""
+    """la_prefill_ws at other feature dimensions, bf16, with an initial state:
+    d' = 8 on the tensor-core kernel (the padded map) at the long-prefill shape
+    B=16, H=16, N=32768; d' = 24, 32 at B=4, H=16, N=4096 with the chunk
+    contractions on the tensor cores (cuBLASLt batched GEMMs and the library's
+    kernels, in the workspace)."""
     out = {}
     for dk in (8, 24, 32):
         D = 1 + dk + dk * dk
@@ -428,14 +431,17 @@ def leg_general_dk(la, args, dist, dev):
         y = torch.empty((B, H, N, 64), dtype=torch.bfloat16, device=dev)
         s = torch.empty_like(s0)
         z = torch.empty_like(z0)
+        need = la.prefill_workspace_size(B, H, N, dk)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
 
         def step():
-            la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z)
+            la.prefill(q, k, v, s0, z0, y=y, s_out=s, z_out=z, workspace=ws)
 
-        ms = time_loop(step, max(1, args.steps // (4 if dk == 8 else 20)), 3, dist)
+        ms = time_loop(step, max(1, args.steps // 4), 3, dist)
         la.check_device_status()
-        out[dk] = {"ms": ms, "B": B, "H": H, "N": N, "D": D,
-                   "path": "tensor cores (padded d' = 16 map)" if dk == 8 else "CUDA cores (general d')"}
+        out[dk] = {"ms": ms, "B": B, "H": H, "N": N, "D": D, "workspace_bytes": need,
+                   "path": "tensor-core kernel (padded d' = 16 map)" if dk == 8 else
+                           "tensor cores: cuBLASLt batched GEMMs + feature, scan, P and y kernels"}
     return out
 
 
@@ -725,8 +731,10 @@ def main():
                 "workload": f"prefill-bf16-B{r['B']}-H{r['H']}-N{r['N']}-dk{dk}-D{r['D']}-s0",
                 "ms_per_call": r["ms"], "tokens_per_s": W * r["B"] * r["N"] / t,
                 "achieved_tflops": fl / t / 1e12, "tc_frac": fl / t / 1e12 / pk["bf16_tflops"],
-                "path": r["path"]}
-            launches += max(1, args.steps // (4 if dk == 8 else 20))
+                "path": r["path"], "workspace_bytes": r["workspace_bytes"]}
+            # the library's own kernels per call (d' = 24, 32: features, scan, P, y;
+            # the three GEMMs are cuBLASLt's)
+            launches += max(1, args.steps // 4) * (1 if dk == 8 else 4)
     suffix = {"decode": "", "decode_decay": "-decay-1-2^-(4+h)", "decode_compact": "-compact-state-153"}
     for dname in ("decode", "decode_decay", "decode_compact"):
         if dname not in res:

@@ -9,7 +9,7 @@ from .binding import (  # noqa: F401
     LA_ERR_SCRATCH_TOO_SMALL, LA_ERR_TIMEOUT, LA_ERR_UNSUPPORTED, LA_OK, LAError, LIB_PATH,
     check_device_status, debug_timeout_probe, decode_step, decode_step_compact, load_library,
     noalloc_scratch_bytes, prefill, prefill_compact, prefill_host, prefill_host_workspace_size,
-    prefill_split_info,
+    prefill_split_info, prefill_workspace_size,
     prefix_prefill, prefix_prefill_noalloc, prefix_workspace_size, state_from_compact,
     state_to_compact, status_string,
 )

@@ -227,6 +227,13 @@ def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
     return y, s_out, z_out
 
 
+def prefill_workspace_size(B: int, H: int, N: int, dk: int = D_FEAT,
+                           dtype: torch.dtype = torch.bfloat16) -> int:
+    """Bytes of the workspace la_prefill_ws uses (0: the call has no use for one)."""
+    dt = LA_DTYPE_BF16 if dtype == torch.bfloat16 else LA_DTYPE_F32
+    return int(load_library().la_prefill_workspace_size(B, H, N, dk, dt))
+
+
 def prefill_split_info(B: int, H: int, N: int):
     """(split_heads, split_chunk) that la_prefill_ws chooses on the current device."""
     r, c = ctypes.c_int(0), ctypes.c_int(0)

@@ -83,7 +83,9 @@ def build(force: bool = False, verbose: bool = False, extra=(), trace: bool = Fa
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(lambda s: _compile(s, verbose, extra, build_dir), srcs))
     tmp = lib + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+    # cuBLASLt (the d' = 24, 32 tensor-core path), found next to the toolkit's nvcc
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
+    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcublasLt", "-Xlinker", "-rpath", "-Xlinker", cuda_lib]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -246,6 +246,10 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
     if ((st = device_setup(&dev, &status)) != LA_OK) return st;
     la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad, gamma};
     a.compact = compact;
+    // d' = 24, 32 (bf16) on the tensor cores, given room for its buffers
+    if (workspace && dtype == LA_DTYPE_BF16 && (d_feat == 24 || d_feat == 32) && N > 0 &&
+        workspace_bytes >= la::general_tc_workspace(BH, N, d_feat))
+        return to_status(la::launch_prefill_general_tc(a, d_feat, workspace, reinterpret_cast<cudaStream_t>(stream)));
     // split heads on the bf16 tensor-core path, given room for the hand-over
     if (workspace && dtype == LA_DTYPE_BF16 && (d_feat == kDFeat || d_feat == 8) &&
         workspace_bytes >= xfer_bytes(BH) + xflag_bytes(BH))
@@ -331,7 +335,9 @@ la_status la_prefill(const void *q, const void *k, const void *v, const float *s
 
 size_t la_prefill_workspace_size(int64_t B, int64_t H, int64_t N, int d_feat, la_dtype dtype) {
     if (B < 1 || H < 1 || N < 0 || B > kMaxBH / H) return 0;
-    if ((d_feat != kDFeat && d_feat != 8) || dtype != LA_DTYPE_BF16) return 0;
+    if (dtype != LA_DTYPE_BF16) return 0;
+    if (d_feat == 24 || d_feat == 32) return la::general_tc_workspace(B * H, N, d_feat);
+    if (d_feat != kDFeat && d_feat != 8) return 0;
     return xfer_bytes(B * H) + xflag_bytes(B * H);
 }
 

@@ -115,6 +115,11 @@ inline PrefixSplit prefix_split(int64_t BH, int64_t M) {
 inline bool supported_dk(int dk) { return dk == 8 || dk == 16 || dk == 24 || dk == 32; }
 inline int64_t feat_dim(int dk) { return 1 + (int64_t)dk + (int64_t)dk * dk; }
 cudaError_t launch_prefill_general(const PrefillArgs &a, int dk, la_dtype dt, cudaStream_t st);
+// d' = 24, 32 with bf16 activations on the tensor cores (cuBLASLt batched GEMMs
+// and this library's kernels), in a workspace of general_tc_workspace bytes
+// (0 for other d' or N = 0).
+size_t general_tc_workspace(int64_t BH, int64_t N, int dk);
+cudaError_t launch_prefill_general_tc(const PrefillArgs &a, int dk, void *workspace, cudaStream_t st);
 cudaError_t launch_decode_general(const DecodeArgs &a, int dk, la_dtype dt, cudaStream_t st);
 
 cudaError_t launch_decode(const DecodeArgs &a, la_dtype dt, cudaStream_t st);

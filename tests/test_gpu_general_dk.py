@@ -91,3 +91,36 @@ def test_dk8_split_heads():
     sel = lambda t: torch.stack([t[i // H, i % H] for i in idx])[None]
     ref = oracle.prefill(sel(q), sel(k), sel(v), sel(s0), sel(z0))
     check((sel(y), sel(s), sel(z)), ref, TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("dk", [24, 32])
+@pytest.mark.parametrize("N", [128, 1000, 2100])
+def test_dk24_32_tensor_core_prefill(dk, N):
+    """bf16 at d' = 24, 32 through la_prefill_ws (the compact symmetric map,
+    chunk states and read-out on the tensor cores): one chunk, ragged chunk
+    counts, a non-symmetric initial state (its antisymmetric part passes
+    through to s_out), against the oracle's full map."""
+    D = oracle.feature_dim(dk)
+    q, k, v, _, _ = inputs.qkv(2, 3, N, seed=1600 + dk + N, dtype=torch.bfloat16, dk=dk)
+    s0, z0 = inputs.random_state(2, 3, seed=1601 + dk, D=D)
+    ws = la.prefill_workspace_size(2, 3, N, dk)
+    assert ws > 0
+    got = la.prefill(q.to(DEV), k.to(DEV), v.to(DEV), s0.to(DEV), z0.to(DEV))
+    torch.cuda.synchronize()
+    la.check_device_status()
+    ref = oracle.prefill(q, k, v, s0, z0)
+    check(got, ref, TOL[torch.bfloat16], f" dk={dk} N={N}")
+
+
+@pytest.mark.parametrize("dk", [24, 32])
+def test_dk24_32_tensor_core_agrees_with_cuda_cores(dk):
+    """The tensor-core path (la_prefill_ws) and the CUDA-core path (la_prefill)
+    on the same bf16 inputs, without an initial state: the same y and state up
+    to bf16 rounding."""
+    q, k, v, _, _ = inputs.qkv(2, 2, 777, seed=1700 + dk, dtype=torch.bfloat16, dk=dk)
+    args = [t.to(DEV) for t in (q, k, v)]
+    a = la.prefill(*args)
+    b = la.prefill(*args, split=False)
+    torch.cuda.synchronize()
+    for name, x, r in zip("ysz", a, b):
+        assert_close(name, x, r.double().cpu().numpy(), 1e-2)
