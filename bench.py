@@ -522,7 +522,9 @@ def ncu_case(la, case: str):
     back (inputs generated first, so that nothing runs between the steps; the
     compact case over the bench leg's independent states in turn);
     prefix N=M=4096, three calls; the decayed prefill (the bench leg's rates)
-    at B=16, H=16, N=8192 with an initial state, two launches (split heads)."""
+    at B=16, H=16, N=8192 with an initial state, two launches (split heads);
+    general_dk: d' = 24 then 32 at the bench leg's B=4, H=16, N=4096 with an
+    initial state, two calls each (7 launches per call)."""
     dev = "cuda:0"
     g = torch.Generator(device=dev)
     g.manual_seed(0)
@@ -564,6 +566,18 @@ def ncu_case(la, case: str):
         gam = decay_rates(H, dev)
         for _ in range(2):
             la.prefill(q, k, v, s0, z0, gamma=gam)
+    elif case == "general_dk":
+        B, H, N = 4, 16, 4096
+        for dk in (24, 32):
+            D = 1 + dk + dk * dk
+            q, k = gen_device((B, H, N, dk), g, dev=dev), gen_device((B, H, N, dk), g, dev=dev)
+            v = gen_device((B, H, N, 64), g, dev=dev)
+            s0 = torch.randn((B, H, D, 64), generator=g, device=dev)
+            z0 = torch.rand((B, H, D), generator=g, device=dev) + 64.0
+            ws = torch.empty(la.prefill_workspace_size(B, H, N, dk), dtype=torch.uint8, device=dev)
+            for _ in range(2):
+                la.prefill(q, k, v, s0, z0, workspace=ws)
+            torch.cuda.synchronize()
     elif case == "prefix":
         B, H, N, M = 16, 16, 4096, 4096
         q, k = gen_device((B, H, N, 16), g, dev=dev), gen_device((B, H, N, 16), g, dev=dev)
@@ -594,7 +608,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-split", action="store_true",
                     help="time la_prefill without the workspace (no split heads in the last wave)")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_compact", "prefix", "prefill_decay"],
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_compact", "prefix", "prefill_decay",
+                                           "general_dk"],
                     help="run one small case for an ncu capture and exit (no timing)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

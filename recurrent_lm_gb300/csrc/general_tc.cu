@@ -53,36 +53,31 @@ struct GDims {
     static constexpr int kD = 1 + DK + DK * DK;             // ABI rows
 };
 
-// Compact feature f: 0xFFFF the constant, a | 0xFF00 the linear feature a,
-// a | b << 8 the product of a <= b (in the order a = 0..d'-1, b = a..d'-1).
+// Compact feature f as a product xe[ia] * xe[ib] * scale over xe = [1, xbar]:
+// the constant (0, 0, 1), linear a (1 + a, 0, 1), square (1 + a, 1 + a,
+// 1/sqrt(2)), pair a < b (1 + a, 1 + b, 1), in the order constant, linear
+// a = 0..d'-1, then a = 0..d'-1, b = a..d'-1; padding features have scale 0.
+// code = ia | ib << 8 | kind << 16 (kind 0: scale 0, 1: scale 1, 2: 1/sqrt(2)).
 template <int DK>
 struct FeatTable {
-    uint16_t code[GDims<DK>::kDc];
+    uint32_t code[GDims<DK>::kDp];
     constexpr FeatTable() : code() {
         int f = 0;
-        code[f++] = 0xFFFF;
-        for (int a = 0; a < DK; ++a) code[f++] = (uint16_t)(a | 0xFF00);
+        code[f++] = 0u | (0u << 8) | (1u << 16);
+        for (int a = 0; a < DK; ++a) code[f++] = (uint32_t)(1 + a) | (0u << 8) | (1u << 16);
         for (int a = 0; a < DK; ++a)
-            for (int b = a; b < DK; ++b) code[f++] = (uint16_t)(a | (b << 8));
+            for (int b = a; b < DK; ++b)
+                code[f++] = (uint32_t)(1 + a) | ((uint32_t)(1 + b) << 8) | ((a == b ? 2u : 1u) << 16);
+        while (f < GDims<DK>::kDp) code[f++] = 0u;
     }
 };
 __device__ const FeatTable<24> kFeat24{};
 __device__ const FeatTable<32> kFeat32{};
 
 template <int DK>
-__device__ __forceinline__ uint16_t feat_code(int f) {
+__device__ __forceinline__ uint32_t feat_code(int f) {
     if constexpr (DK == 24) return __ldg(&kFeat24.code[f]);
     else return __ldg(&kFeat32.code[f]);
-}
-
-template <int DK>
-__device__ __forceinline__ float feat_value(const float *x, int f) {
-    if (f >= GDims<DK>::kDc) return 0.f;
-    const uint16_t c = feat_code<DK>(f);
-    if (c == 0xFFFF) return 1.f;
-    const int a = c & 0xFF, b = c >> 8;
-    if (b == 0xFF) return x[a];
-    return a == b ? x[a] * x[a] * kInvSqrt2 : x[a] * x[b];
 }
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 h) { return __bfloat162float(h); }
@@ -92,38 +87,73 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&p);
 }
 
-// 1. One warp per token (bh, t), t < Np = chunks * 128: the query and key
-// features and [v | 1 | 0], all zero for t >= N.
+// 1. A CTA per 32 tokens (of Np = chunks * 128 per head): the query and key
+// features (each thread 8 consecutive features of one token, one 16-byte
+// store per side: a warp's stores cover consecutive 16-byte pieces of a
+// token's rows) and [v | 1 | 0], all zero for t >= N.
+constexpr int kFT = 32;  // tokens per CTA
 template <int DK>
 __global__ void __launch_bounds__(256) feat_kernel(const __nv_bfloat16 *__restrict__ q,
                                                    const __nv_bfloat16 *__restrict__ k,
-                                                   const __nv_bfloat16 *__restrict__ v, uint32_t *__restrict__ phq,
-                                                   uint32_t *__restrict__ phk, uint32_t *__restrict__ ve,
-                                                   int64_t BH, int64_t N, int64_t Np, float xscale) {
-    constexpr int Dp = GDims<DK>::kDp;
-    __shared__ float xs[8][2][DK];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tok = (int64_t)blockIdx.x * 8 + warp;
-    if (tok >= BH * Np) return;
-    const int64_t bh = tok / Np, t = tok % Np;
-    const bool in = t < N;
-    if (lane < DK) {
-        xs[warp][0][lane] = in ? xscale * bf2f(q[(bh * N + t) * DK + lane]) : 0.f;
-        xs[warp][1][lane] = in ? xscale * bf2f(k[(bh * N + t) * DK + lane]) : 0.f;
+                                                   const __nv_bfloat16 *__restrict__ v, uint4 *__restrict__ phq,
+                                                   uint4 *__restrict__ phk, uint4 *__restrict__ ve,
+                                                   int64_t N, int64_t Np, float xscale) {
+    constexpr int Dp = GDims<DK>::kDp, G = Dp / 8, XE = DK + 1;
+    __shared__ float xq[kFT][XE], xk[kFT][XE];
+    __shared__ __align__(16) uint32_t code[Dp];
+    const int tid = threadIdx.x;
+    // the CTA's 32 tokens lie in one head (Np is a multiple of 128)
+    const int64_t tok0 = (int64_t)blockIdx.x * kFT;  // first token (bh * Np + t)
+    const int64_t bh = tok0 / Np, t0 = tok0 % Np;
+    for (int f = tid; f < Dp; f += blockDim.x) code[f] = feat_code<DK>(f);
+    for (int e = tid; e < kFT * XE; e += blockDim.x) {
+        const int r = e / XE, c = e % XE;
+        const int64_t t = t0 + r;
+        float xqv = 0.f, xkv = 0.f;
+        if (c == 0) {
+            xqv = xkv = 1.f;
+        } else if (t < N) {
+            xqv = xscale * bf2f(q[(bh * N + t) * DK + c - 1]);
+            xkv = xscale * bf2f(k[(bh * N + t) * DK + c - 1]);
+        }
+        xq[r][c] = xqv;
+        xk[r][c] = xkv;
     }
-    __syncwarp();
-    uint32_t *oq = phq + tok * (Dp / 2), *ok = phk + tok * (Dp / 2);
-    for (int j = lane; j < Dp / 2; j += 32) {
-        const int f = 2 * j;
-        oq[j] = in ? pack2(feat_value<DK>(xs[warp][0], f), feat_value<DK>(xs[warp][0], f + 1)) : 0u;
-        ok[j] = in ? pack2(feat_value<DK>(xs[warp][1], f), feat_value<DK>(xs[warp][1], f + 1)) : 0u;
+    __syncthreads();
+    for (int it = tid; it < kFT * G; it += blockDim.x) {
+        const int r = it / G, g = it % G;
+        const int64_t tok = tok0 + r;
+        const bool in = t0 + r < N;
+        const uint4 c0 = *reinterpret_cast<const uint4 *>(&code[8 * g]);
+        const uint4 c1 = *reinterpret_cast<const uint4 *>(&code[8 * g + 4]);
+        const uint32_t cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t wq[4], wk[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float oq[2], ok[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const uint32_t c = cs[2 * h + e];
+                const int ia = c & 0xFF, ib = (c >> 8) & 0xFF, kind = c >> 16;
+                const float sc = kind == 0 ? 0.f : (kind == 1 ? 1.f : kInvSqrt2);
+                oq[e] = xq[r][ia] * xq[r][ib] * sc;
+                ok[e] = xk[r][ia] * xk[r][ib] * sc;
+            }
+            wq[h] = in ? pack2(oq[0], oq[1]) : 0u;
+            wk[h] = in ? pack2(ok[0], ok[1]) : 0u;
+        }
+        phq[tok * G + g] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        phk[tok * G + g] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
     }
-    uint32_t *ov = ve + tok * (kNV / 2);
-    for (int j = lane; j < kNV / 2; j += 32) {
-        uint32_t w = 0u;
-        if (in && 2 * j < kDV) w = *reinterpret_cast<const uint32_t *>(v + (bh * N + t) * kDV + 2 * j);
-        else if (in && 2 * j == kDV) w = pack2(1.f, 0.f);  // the ones column (z) and a zero
-        ov[j] = w;
+    for (int it = tid; it < kFT * (kNV / 8); it += blockDim.x) {
+        const int r = it / (kNV / 8), g = it % (kNV / 8);
+        const int64_t tok = tok0 + r, t = t0 + r;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (t < N) {
+            if (g < kDV / 8) w = reinterpret_cast<const uint4 *>(v + (bh * N + t) * kDV)[g];
+            else if (g == kDV / 8) w.x = pack2(1.f, 0.f);  // the ones column (z)
+        }
+        ve[tok * (kNV / 8) + g] = w;
     }
 }
 
@@ -146,11 +176,12 @@ __global__ void __launch_bounds__(256) scan_kernel(const float *__restrict__ dS,
     // ABI rows of feature f: r1 (and r2 for a pair a < b: rows ab and ba)
     int r1 = 0, r2 = -1;
     if (f < Dc) {
-        const uint16_t c = feat_code<DK>(f);
-        const int a = c & 0xFF, b = c >> 8;
-        if (c == 0xFFFF) r1 = 0;
-        else if (b == 0xFF) r1 = 1 + a;
+        const uint32_t c = feat_code<DK>(f);
+        const int ia = c & 0xFF, ib = (c >> 8) & 0xFF;  // indices into [1, xbar]
+        if (ia == 0) r1 = 0;                            // the constant
+        else if (ib == 0) r1 = ia;                      // linear: row 1 + a
         else {
+            const int a = ia - 1, b = ib - 1;
             r1 = 1 + DK + a * DK + b;
             if (a != b) r2 = 1 + DK + b * DK + a;
         }
@@ -194,49 +225,71 @@ __global__ void __launch_bounds__(256) scan_kernel(const float *__restrict__ dS,
 
 // 5. One CTA per (bh, chunk): P[i][j] = 1 + T/sqrt(d') + T^2/(2 d') for
 // j <= i, else 0, T = q_i . k_j in fp32 from the bf16 inputs (rows past N read
-// as zero: their P entries meet zero rows of [v | 1]).  Thread t: query row
-// t / 2, keys 64 (t % 2) .. + 63, written as 8 x 16 bytes.
+// as zero: their P entries meet zero rows of [v | 1]).  Thread t: an 8 x 8
+// tile of (i, j), queries 8 (t / 16), keys 8 (t % 16), from d'-major copies
+// of Q and K in shared memory (two 16-byte reads feed 64 FMAs).
 template <int DK>
 __global__ void __launch_bounds__(256) intra_p_kernel(const __nv_bfloat16 *__restrict__ q,
                                                       const __nv_bfloat16 *__restrict__ k,
                                                       uint4 *__restrict__ P, int64_t N, int nch) {
-    __shared__ float ks[kCG][DK + 1];
-    __shared__ float qs[kCG][DK + 1];
+    __shared__ __align__(16) float qs[DK][kCG];
+    __shared__ __align__(16) float ks[DK][kCG];
     const int64_t bc = blockIdx.x;
     const int64_t bh = bc / nch;
     const int c = (int)(bc % nch);
     const int tid = threadIdx.x;
-    for (int e = tid; e < kCG * DK; e += blockDim.x) {
-        const int t = e / DK, dd = e % DK;
+    // thread: 8 dims of one token (16 bytes); a warp's smem writes go to 32
+    // consecutive tokens of a row, conflict-free
+    for (int e = tid; e < kCG * (DK / 8); e += blockDim.x) {
+        const int t = e % kCG, d8 = e / kCG;
         const int64_t tok = (int64_t)c * kCG + t;
-        const bool in = tok < N;
-        qs[t][dd] = in ? bf2f(q[(bh * N + tok) * DK + dd]) : 0.f;
-        ks[t][dd] = in ? bf2f(k[(bh * N + tok) * DK + dd]) : 0.f;
+        uint4 wq = make_uint4(0u, 0u, 0u, 0u), wk = wq;
+        if (tok < N) {
+            wq = reinterpret_cast<const uint4 *>(q + (bh * N + tok) * DK)[d8];
+            wk = reinterpret_cast<const uint4 *>(k + (bh * N + tok) * DK)[d8];
+        }
+        const uint32_t aq[4] = {wq.x, wq.y, wq.z, wq.w}, ak[4] = {wk.x, wk.y, wk.z, wk.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            qs[8 * d8 + 2 * h][t] = __uint_as_float(aq[h] << 16);
+            qs[8 * d8 + 2 * h + 1][t] = __uint_as_float(aq[h] & 0xFFFF0000u);
+            ks[8 * d8 + 2 * h][t] = __uint_as_float(ak[h] << 16);
+            ks[8 * d8 + 2 * h + 1][t] = __uint_as_float(ak[h] & 0xFFFF0000u);
+        }
     }
     __syncthreads();
-    const int i = tid >> 1, j0 = (tid & 1) * 64;
-    float qr[DK];
+    const int i0 = 8 * (tid >> 4), j0 = 8 * (tid & 15);
+    float T[8][8];
 #pragma unroll
-    for (int dd = 0; dd < DK; ++dd) qr[dd] = qs[i][dd];
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) T[a][b] = 0.f;
+#pragma unroll 4
+    for (int dd = 0; dd < DK; ++dd) {
+        const float4 qa = *reinterpret_cast<const float4 *>(&qs[dd][i0]);
+        const float4 qb = *reinterpret_cast<const float4 *>(&qs[dd][i0 + 4]);
+        const float4 ka = *reinterpret_cast<const float4 *>(&ks[dd][j0]);
+        const float4 kb = *reinterpret_cast<const float4 *>(&ks[dd][j0 + 4]);
+        const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        const float kv[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+#pragma unroll
+            for (int b = 0; b < 8; ++b) T[a][b] = fmaf(qv[a], kv[b], T[a][b]);
+    }
     const float c1 = rsqrtf((float)DK), c2 = 0.5f / (float)DK;
-    uint4 *row = P + (bc * kCG + i) * (kCG / 8) + j0 / 8;
-#pragma unroll 1
-    for (int g = 0; g < 8; ++g) {
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        const int i = i0 + a;
         uint32_t w[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-            float p2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int j = j0 + 8 * g + 2 * h + e;
-                float T = 0.f;
-#pragma unroll
-                for (int dd = 0; dd < DK; ++dd) T = fmaf(qr[dd], ks[j][dd], T);
-                p2[e] = j <= i ? fmaf(T, fmaf(T, c2, c1), 1.f) : 0.f;
-            }
-            w[h] = pack2(p2[0], p2[1]);
+            const int j = j0 + 2 * h;
+            const float p0 = j <= i ? fmaf(T[a][2 * h], fmaf(T[a][2 * h], c2, c1), 1.f) : 0.f;
+            const float p1 = j + 1 <= i ? fmaf(T[a][2 * h + 1], fmaf(T[a][2 * h + 1], c2, c1), 1.f) : 0.f;
+            w[h] = pack2(p0, p1);
         }
-        row[g] = make_uint4(w[0], w[1], w[2], w[3]);
+        P[(bc * kCG + i) * (kCG / 8) + j0 / 8] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -359,9 +412,9 @@ cudaError_t run_general_tc(const PrefillArgs &a, char *ws, cudaStream_t st) {
     const float xscale = 1.0f / sqrtf(sqrtf((float)DK));
     const int batch = (int)(BH * nch);
 
-    feat_kernel<DK><<<(unsigned)((BH * Np + 7) / 8), 256, 0, st>>>(
-        q, k, v, reinterpret_cast<uint32_t *>(phq), reinterpret_cast<uint32_t *>(phk),
-        reinterpret_cast<uint32_t *>(ve), BH, N, Np, xscale);
+    feat_kernel<DK><<<(unsigned)(BH * Np / kFT), 256, 0, st>>>(
+        q, k, v, reinterpret_cast<uint4 *>(phq), reinterpret_cast<uint4 *>(phk), reinterpret_cast<uint4 *>(ve), N,
+        Np, xscale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // 2. dS_c (Dp x 80, row-major) = Phi_Kc^T [V_c | 1]: column-major 80 x Dp = [V_c | 1]^T Phi_Kc
