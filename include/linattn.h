@@ -117,13 +117,25 @@ LA_API la_status la_prefill(const void *q, const void *k, const void *v,
  * la_prefill up to fp32 rounding order in the handed-over state; they are
  * reproducible on a given device (the split depends on its SM count).
  *
+ * With bf16 activations and d_feat = 24 or 32, the workspace instead holds
+ * the buffers of a chunked form whose contractions run on the tensor cores
+ * (the same blockwise form, BASED notes sec. 2.5, with the symmetric compact
+ * feature map of sec. 2.3 for that d': 325 or 561 features; the chunk states,
+ * the read-out and the intra-chunk products are cuBLASLt batched GEMMs with
+ * bf16 operands and fp32 accumulation).  Its results equal la_prefill's up to
+ * bf16 rounding (the states before each chunk are rounded to bf16 for the
+ * read-out); the final state's antisymmetric part is s0's, passed through.
+ * That workspace is large: about 3.3 KB (d' = 24) or 5.1 KB (d' = 32) per
+ * (b, h) token of ceil(N / 128) * 128 tokens, plus 32 MB.
+ *
  *   workspace: DEVICE buffer of at least la_prefill_workspace_size(B, H, N,
  *   d_feat, dtype) bytes, 256-byte aligned, owned by the caller, not read
  *   before written.  It must not be used by two calls whose work overlaps on
  *   the GPU.  NULL, or too small, runs exactly la_prefill.
  * All other arguments, layouts and errors are those of la_prefill (padding and
- * decay have no workspace form).  la_prefill_workspace_size returns 0 where no
- * split is possible (fp32 activations, d_feat != 16).
+ * decay have no workspace form at d_feat != 16).  la_prefill_workspace_size
+ * returns 0 where the workspace has no use (fp32 activations; N = 0 at
+ * d_feat 24, 32).
  */
 LA_API size_t la_prefill_workspace_size(int64_t B, int64_t H, int64_t N, int d_feat, la_dtype dtype);
 /* The split la_prefill_ws (and the prefix call) make on the current device for
