@@ -209,6 +209,22 @@ def test_host_prefill_workspace_size(lib):
     assert lib.la_prefill_host_workspace_size(2, 3, 300, 16, 1) < lib.la_prefill_host_workspace_size(2, 3, 300, 16, 0)
 
 
+def test_prefill_workspace_size_general_dk(lib):
+    """d' = 24, 32 with bf16 (dtype 1): the workspace of the tensor-core form,
+    at least its buffers per token of whole 128-token chunks (features of q and
+    k, [v | 1 | 0], chunk states in fp32 and bf16, the numerator, P) plus the
+    cuBLASLt workspace; none for fp32 or an empty sequence."""
+    for dk, dp in ((24, 328), (32, 568)):
+        B, H, N = 2, 3, 300
+        tokens = B * H * 384  # three chunks
+        per_token = 2 * 2 * dp + 2 * 80 + (4 + 2) * dp * 80 / 128 + 4 * 80 + 2 * 128
+        need = lib.la_prefill_workspace_size(B, H, N, dk, 1)
+        assert tokens * per_token + (32 << 20) <= need <= tokens * per_token + (32 << 20) + 8 * 256
+        assert lib.la_prefill_workspace_size(B, H, N, dk, 0) == 0
+        assert lib.la_prefill_workspace_size(B, H, 0, dk, 1) == 0
+    assert lib.la_prefill_workspace_size(2, 3, 300, 12, 1) == 0
+
+
 def call_host(lib, p, ws, ws_bytes, B=2, H=3, N=300, dk=16, dtype=1):
     return lib.la_prefill_host(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], ws, ws_bytes, B, H, N,
                                dk, 64, dtype, 0.0, None)

@@ -124,3 +124,19 @@ def test_dk24_32_tensor_core_agrees_with_cuda_cores(dk):
     torch.cuda.synchronize()
     for name, x, r in zip("ysz", a, b):
         assert_close(name, x, r.double().cpu().numpy(), 1e-2)
+
+
+def test_dk24_small_workspace_runs_the_cuda_core_path():
+    """la_prefill_ws with a workspace one byte short of la_prefill_workspace_size
+    runs exactly la_prefill (the CUDA-core path): bitwise the same outputs."""
+    dk = 24
+    q, k, v, _, _ = inputs.qkv(1, 2, 300, seed=1800, dtype=torch.bfloat16, dk=dk)
+    s0, z0 = inputs.random_state(1, 2, seed=1801, D=oracle.feature_dim(dk))
+    args = [t.to(DEV) for t in (q, k, v, s0, z0)]
+    need = la.prefill_workspace_size(1, 2, 300, dk)
+    short = torch.empty(need - 1, dtype=torch.uint8, device=DEV)
+    a = la.prefill(*args, workspace=short)
+    b = la.prefill(*args, split=False)
+    torch.cuda.synchronize()
+    for x, r in zip(a, b):
+        assert torch.equal(x, r)
