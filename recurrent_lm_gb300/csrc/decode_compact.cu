@@ -48,7 +48,7 @@ __device__ __forceinline__ float phi_c_feature(const float *xbar, int f) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 4)
 decode_compact_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                       const float *s_in, const float *z_in, float *s_out, float *z_out,
                       T *__restrict__ y, float eps) {
