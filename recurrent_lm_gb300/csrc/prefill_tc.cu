@@ -162,7 +162,11 @@ __device__ __forceinline__ void convert_groups(uint32_t taddr, uint32_t sbase, i
         // rescaled in place and written back with one store and one wait
         __syncwarp();  // tcgen05.st is warp-collective
 #pragma unroll
-        for (int j = 0; j < 32 * kNG; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * decay);
+        for (int j = 0; j < 16 * kNG; ++j) {  // packed fp32x2 multiplies
+            const uint64_t p = fmul2((uint64_t)r[2 * j] | ((uint64_t)r[2 * j + 1] << 32), f2pack(decay, decay));
+            r[2 * j] = (uint32_t)p;
+            r[2 * j + 1] = (uint32_t)(p >> 32);
+        }
         if constexpr (kNG == 2)
             tmem_store64_sync(taddr + 32 * kG0, reinterpret_cast<const uint32_t (&)[64]>(r));
         else
