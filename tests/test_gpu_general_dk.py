@@ -140,3 +140,34 @@ def test_dk24_small_workspace_runs_the_cuda_core_path():
     torch.cuda.synchronize()
     for x, r in zip(a, b):
         assert torch.equal(x, r)
+
+
+@pytest.mark.parametrize("dk", [24, 32])
+def test_dk24_32_tensor_core_bench_size_sampled_heads(dk):
+    """The bench leg's workload (B=4, H=16, N=4096 with s0) through the
+    tensor-core form in one call; three sampled heads (first, middle, last) of
+    y and the final state against the oracle."""
+    B, H, N = 4, 16, 4096
+    D = oracle.feature_dim(dk)
+    q, k, v, _, _ = inputs.qkv(B, H, N, seed=1900 + dk, dtype=torch.bfloat16, dk=dk)
+    s0, z0 = inputs.random_state(B, H, seed=1901 + dk, D=D)
+    y, s, z = la.prefill(q.to(DEV), k.to(DEV), v.to(DEV), s0.to(DEV), z0.to(DEV))
+    torch.cuda.synchronize()
+    la.check_device_status()
+    idx = [0, (B * H) // 2 + 3, B * H - 1]
+    sel = lambda t: torch.stack([t[i // H, i % H] for i in idx])[None]
+    ref = oracle.prefill(sel(q), sel(k), sel(v), sel(s0), sel(z0))
+    check((sel(y), sel(s), sel(z)), ref, TOL[torch.bfloat16], f" dk={dk}")
+
+
+@pytest.mark.parametrize("dk", [24, 32])
+def test_dk24_32_tensor_core_without_states(dk):
+    """No initial state and no state outputs (NULL s0/z0 and s_out/z_out):
+    y against the oracle from a zero state."""
+    q, k, v, _, _ = inputs.qkv(2, 2, 640, seed=2000 + dk, dtype=torch.bfloat16, dk=dk)
+    y, s, z = la.prefill(q.to(DEV), k.to(DEV), v.to(DEV), want_state=False)
+    torch.cuda.synchronize()
+    la.check_device_status()
+    assert s is None and z is None
+    yr, _, _ = oracle.prefill(q, k, v)
+    assert_close("y", y, yr, TOL[torch.bfloat16])
