@@ -442,7 +442,10 @@ cudaError_t run_general_tc(const PrefillArgs &a, char *ws, cudaStream_t st) {
 }  // namespace
 
 size_t general_tc_workspace(int64_t BH, int64_t N, int dk) {
-    if ((dk != 24 && dk != 32) || N <= 0) return 0;
+    if ((dk != 24 && dk != 32) || N <= 0 || BH <= 0) return 0;
+    // every grid and the GEMMs' batch count fit 32 bits while B*H*Np <= 2^31
+    const int64_t Np = (N + kCG - 1) / kCG * kCG;
+    if (BH > (int64_t(1) << 31) / Np) return 0;
     return g_layout(BH, N, dk).total;
 }
 

@@ -247,9 +247,12 @@ la_status prefill_impl(const void *q, const void *k, const void *v, const float 
     la::PrefillArgs a{q, k, v, s0, z0, y, s_out, z_out, B, H, N, eps, status, left_pad, gamma};
     a.compact = compact;
     // d' = 24, 32 (bf16) on the tensor cores, given room for its buffers
-    if (workspace && dtype == LA_DTYPE_BF16 && (d_feat == 24 || d_feat == 32) && N > 0 &&
-        workspace_bytes >= la::general_tc_workspace(BH, N, d_feat))
-        return to_status(la::launch_prefill_general_tc(a, d_feat, workspace, reinterpret_cast<cudaStream_t>(stream)));
+    if (workspace && dtype == LA_DTYPE_BF16 && (d_feat == 24 || d_feat == 32)) {
+        const size_t need = la::general_tc_workspace(BH, N, d_feat);  // 0: not this path
+        if (need > 0 && workspace_bytes >= need)
+            return to_status(
+                la::launch_prefill_general_tc(a, d_feat, workspace, reinterpret_cast<cudaStream_t>(stream)));
+    }
     // split heads on the bf16 tensor-core path, given room for the hand-over
     if (workspace && dtype == LA_DTYPE_BF16 && (d_feat == kDFeat || d_feat == 8) &&
         workspace_bytes >= xfer_bytes(BH) + xflag_bytes(BH))
