@@ -225,8 +225,8 @@ def test_prefill_workspace_size_general_dk(lib):
     assert lib.la_prefill_workspace_size(2, 3, 300, 12, 1) == 0
     # past 2^31 head-tokens (whole chunks) the form is not offered: la_prefill_ws
     # then runs la_prefill
-    assert lib.la_prefill_workspace_size(1 << 12, 16, 1 << 15, 24, 1) == 0
-    assert lib.la_prefill_workspace_size(1 << 12, 16, (1 << 15) - 128, 24, 1) > 0
+    assert lib.la_prefill_workspace_size(1 << 12, 16, (1 << 15) + 1, 24, 1) == 0
+    assert lib.la_prefill_workspace_size(1 << 12, 16, 1 << 15, 24, 1) > 0
 
 
 def call_host(lib, p, ws, ws_bytes, B=2, H=3, N=300, dk=16, dtype=1):
