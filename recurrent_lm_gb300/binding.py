@@ -165,7 +165,10 @@ def prefill(q, k, v, s0=None, z0=None, *, eps: float = 0.0, y=None, s_out=None,
     [0, 1] (la_prefill_decay), or None; not combined with left_pad.
     Without either, the call is la_prefill_ws with ``workspace`` (a CUDA uint8
     tensor of la_prefill_workspace_size bytes; allocated here if None), or
-    la_prefill when split is False.
+    la_prefill when split is False.  With bf16 and d' = 24 or 32 that workspace
+    holds the tensor-core form's buffers (about 3.3 or 5.1 KB per head-token,
+    e.g. 0.9 / 1.4 GB at B=4, H=16, N=4096); split=False runs the CUDA-core
+    path, which needs none.
     Returns (y, s_out, z_out); the states are None when want_state is False."""
     lib = load_library()
     B, H, N, dk = q.shape
