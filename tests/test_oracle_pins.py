@@ -52,10 +52,26 @@ def test_phi_explicit_entries():
             assert p[17 + 16 * a + b] == pytest.approx(xb[a] * xb[b] / math.sqrt(2), rel=1e-15)
 
 
+@pytest.mark.parametrize("dk", [8, 24, 32])
+def test_phi_explicit_entries_general_dk(dk):
+    """The same map at other d' (the pages' feature-dimension ablations):
+    1 + d' + d'^2 entries, xbar = x / d'^(1/4), quadratic entry (a, b) at row
+    1 + d' + a d' + b."""
+    x = rnd(dk)
+    p = oracle.phi(x)
+    xb = x / dk ** 0.25
+    assert p.shape == (1 + dk + dk * dk,)
+    assert p[0] == 1.0
+    assert np.allclose(p[1:1 + dk], xb, rtol=1e-15, atol=0)
+    for a in (0, dk // 2, dk - 1):
+        for b in (0, dk // 3, dk - 1):
+            assert p[1 + dk + dk * a + b] == pytest.approx(xb[a] * xb[b] / math.sqrt(2), rel=1e-14)
+
+
 def test_phi_kernel_identity():
     """BASED sec. 2.3: phi(qbar).phi(kbar) = 1 + q.k/sqrt(d') + (q.k)^2/(2d')
-    on 10^4 random pairs (d' = 16) and for d' in {1, 2, 8}."""
-    for dk, n in ((16, 10000), (1, 500), (2, 500), (8, 500)):
+    on 10^4 random pairs (d' = 16) and for d' in {1, 2, 8, 24, 32}."""
+    for dk, n in ((16, 10000), (1, 500), (2, 500), (8, 500), (24, 300), (32, 300)):
         q = rnd(n, dk)
         k = rnd(n, dk)
         lhs = np.array([oracle.phi(q[i]) @ oracle.phi(k[i]) for i in range(n)])
