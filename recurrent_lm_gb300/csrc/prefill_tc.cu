@@ -395,13 +395,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
     }
     const int64_t bh = bh_;
-    const int c0 = c0_;   // first chunk of this CTA's work
-    const int n = n_;     // chunks of this CTA's work
     const int piece = piece_;
-    float *xs = piece ? xfer + (bh - (bh_total - split_r)) * (int64_t)kXferFloats : nullptr;
-    unsigned long long *xf = piece ? xflag + (bh - (bh_total - split_r)) : nullptr;
     // leading padding positions of this batch row: no contribution to any sum, y = 0
     const int lpad = kPad ? (int)row_left_pad(left_pad, bh / H, N, status, tid == 0) : 0;
+    // chunks that lie entirely in the left padding add nothing to the state:
+    // a CTA whose chunks start there skips them (keeping at least one chunk)
+    // and only writes their y, as zeros (the y warps, before their loop)
+    const int skip = kPad ? max(0, min(lpad / kC - c0_, n_ - 1)) : 0;
+    const int c0 = c0_ + skip;  // first chunk of this CTA's work
+    const int n = n_ - skip;    // chunks of this CTA's work
+    float *xs = piece ? xfer + (bh - (bh_total - split_r)) * (int64_t)kXferFloats : nullptr;
+    unsigned long long *xf = piece ? xflag + (bh - (bh_total - split_r)) : nullptr;
     // per-head columns of the state in memory (the 273-row layout, or with
     // kCompact the 153-row one): entry (row r, value d) at [r * 64 + d]
     constexpr int64_t kRowsIO = kCompact ? kDCompact : (kDk == 8 ? 73 : kD);
@@ -868,6 +872,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         const int w = warp - 12;
         const int i = 32 * w + lane;          // query row (num lane)
         const uint32_t lanebase = (uint32_t)(32 * w) << 16;
+        if constexpr (kPad) {
+            if (skip > 0) {  // y of the skipped (fully padded) chunks: zero tiles of this warp's 32 rows
+                const uint32_t stage = sb + kSmY + (uint32_t)w * 4096;
+                for (int j = lane; j < 4096 / 16; j += 32) st_shared_v4(stage + 16u * (uint32_t)j, 0u, 0u, 0u, 0u);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (int c = c0 - skip; c < c0; ++c)
+                        if (c * kC + 32 * w < N) tma_store_3d(&ty, stage, 0, c * kC + 32 * w, (int)bh);
+                    bulk_commit();  // the loop's first bulk_wait_read0 covers these reads of the tile
+                }
+                __syncwarp();
+            }
+        }
         // PV_READY(c) from the y warps: num drained after chunk c - 1, and (one
         // lane) the loads P V(c) and Q K^T(c + 1) read.  The lane observes those
         // loads before it waits for the numerator (they have landed long before),
