@@ -67,6 +67,9 @@ __device__ uint32_t g_ptrace[3][kPTraceChunks][4];
 #define LA_PTR(role, c, ev) do { } while (0)
 #endif
 
+// kPad: the launch carries left-padding counts (a separate instantiation, so
+// the unpadded one carries none of the skip code).
+template <bool kPad>
 __global__ void __launch_bounds__(kThreads, 2)
 prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                          int M, int seg_len, int nseg, float *__restrict__ part_s,
@@ -85,11 +88,15 @@ prefix_partial_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_co
 #ifdef LA_TRACE
     const long long t_start = clock64();
 #endif
-    const int j0 = seg * seg_len;
-    const int j1 = min(M, j0 + seg_len);
-    const int n = (j1 - j0 + kC - 1) / kC;
+    const int js = seg * seg_len;  // the segment: prefix positions [js, j1)
+    const int j1 = min(M, js + seg_len);
     // prefix positions below min(left pad, M) are padding (range reported by the prefill)
     const int pe = (int)min((int64_t)M, row_left_pad(left_pad, bh / H, N, status, false));
+    // the segment's whole chunks below pe add nothing and are skipped (a segment
+    // that is all padding runs no chunk and writes a zero partial state)
+    const int skip = kPad ? max(0, min((pe - js) / kC, (j1 - js + kC - 1) / kC)) : 0;
+    const int j0 = js + skip * kC;               // first chunk processed
+    const int n = (j1 - js + kC - 1) / kC - skip;  // chunks processed
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -246,15 +253,18 @@ cudaError_t launch_prefix_partials_tc(const PrefixArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_for != dev) {
-        cudaError_t e = cudaFuncSetAttribute(prefix_partial_tc_kernel,
+        cudaError_t e = cudaFuncSetAttribute(prefix_partial_tc_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefix_partial_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmAlloc);
         if (e != cudaSuccess) return e;
         configured_for = dev;
     }
     dim3 grid((unsigned)BH, (unsigned)a.nseg);
-    prefix_partial_tc_kernel<<<grid, kThreads, kSmAlloc, st>>>(tk, tv, (int)a.M, (int)a.seg_len,
-                                                               (int)a.nseg, a.part_s, a.part_z, a.status,
-                                                               a.left_pad, a.H, a.N);
+    auto kern = a.left_pad ? prefix_partial_tc_kernel<true> : prefix_partial_tc_kernel<false>;
+    kern<<<grid, kThreads, kSmAlloc, st>>>(tk, tv, (int)a.M, (int)a.seg_len, (int)a.nseg, a.part_s, a.part_z,
+                                           a.status, a.left_pad, a.H, a.N);
     return cudaGetLastError();
 }
 
